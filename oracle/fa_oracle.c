@@ -1,0 +1,359 @@
+/*
+ * fa_oracle.c -- plain FP64 reference for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link,
+ * load or call this file; only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header, table or
+ * constant with the CUDA path.
+ *
+ * What it computes is the textbook definition, written out with no tiling,
+ * no fusion and no reordering:
+ *
+ *   s_ij = scale * <q_i, k_j>                 (FlashAttention_01 page, 3.1 and
+ *                                              the "Flash Attention" history
+ *                                              page, 1.1: softmax(QK^T/sqrt d)V)
+ *   visible(i, j) <=> k_start[b] <= j < k_end[b]  and  (!causal or j <= i + Sk - Sq)
+ *   m   = max over visible j of s_ij          (mask applied before the max,
+ *   l   = sum_vis exp(s_ij - m)                FlashAttention_01 page, "online
+ *   u   = sum_vis exp(s_ij - m) v_j            softmax derivation": m, l, u)
+ *   O_i = u / l,  LSE_i = m + ln l
+ *   no visible key: O_i = 0, LSE_i = -inf, m = -inf, l = 0 (no -inf - -inf
+ *   is ever evaluated; the page asks for an explicit rule).
+ *
+ * Backward (FlashAttention_01 page, "backward recomputation" and the
+ * "attention backward chain rule" section), with dO given:
+ *   p_ij  = exp(s_ij - m_i) / l_i on visible entries, 0 elsewhere
+ *   D_i   = sum_c dO_ic O_ic
+ *   dP_ij = <dO_i, v_j>
+ *   dS_ij = p_ij (dP_ij - D_i)
+ *   dV_j  = sum_i p_ij dO_i
+ *   dQ_i  = scale sum_j dS_ij k_j
+ *   dK_j  = scale sum_i dS_ij q_i
+ * With grouped K/V heads (GQA, "Flash Attention" practitioner page, 2.3)
+ * query head h reads KV head h / (Hq/Hkv), and dK/dV of a KV head sum over
+ * the query heads that read it.
+ *
+ * Inputs are either fp64 arrays or bf16 bit patterns (uint16); a bf16 value
+ * is widened to fp64 exactly.  Layout is [B, H, S, d], d innermost.
+ * OpenMP only distributes independent rows (or independent key rows for
+ * dK/dV); every sum is evaluated in plain index order.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* exact bf16 -> fp64: a bf16 value is the top 16 bits of an IEEE binary32 */
+static double bf16_bits_to_double(uint16_t h) {
+  uint32_t w = ((uint32_t)h) << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+typedef struct {
+  const void* p;
+  int bf16;
+} src_t;
+
+static double ld(src_t s, long idx) {
+  if (s.bf16) return bf16_bits_to_double(((const uint16_t*)s.p)[idx]);
+  return ((const double*)s.p)[idx];
+}
+
+static void load_row(src_t s, long base, long d, double* out) {
+  for (long c = 0; c < d; ++c) out[c] = ld(s, base + c);
+}
+
+static int is_visible(long i, long j, long Sq, long Sk, int causal, long ks, long ke) {
+  if (j < ks || j >= ke) return 0;
+  if (causal && j > i + Sk - Sq) return 0;
+  return 1;
+}
+
+static void key_range(const int* k_start, const int* k_end, long b, long Sk, long* ks, long* ke) {
+  *ks = k_start ? (long)k_start[b] : 0;
+  *ke = k_end ? (long)k_end[b] : Sk;
+}
+
+/*
+ * One query row against n keys.  qrow[d]; key row j starts at index
+ * kbase + j*d in k (and vbase + j*d in v).  Writes m, l, u[d], o[d], lse.
+ * s is caller scratch of length >= n.
+ */
+static void row_attention(const double* qrow, src_t k, long kbase, src_t v, long vbase,
+                          long n, long d, double scale, long i, long Sq, int causal,
+                          long ks, long ke, double* s, double* m_out, double* l_out,
+                          double* u, double* o, double* lse_out) {
+  double m = -INFINITY;
+  long nvis = 0;
+  for (long j = 0; j < n; ++j) {
+    if (!is_visible(i, j, Sq, n, causal, ks, ke)) continue;
+    double acc = 0.0;
+    for (long c = 0; c < d; ++c) acc += qrow[c] * ld(k, kbase + j * d + c);
+    s[j] = scale * acc;
+    if (s[j] > m) m = s[j];
+    ++nvis;
+  }
+  for (long c = 0; c < d; ++c) u[c] = 0.0;
+  if (nvis == 0) {
+    *m_out = -INFINITY;
+    *l_out = 0.0;
+    for (long c = 0; c < d; ++c) o[c] = 0.0;
+    *lse_out = -INFINITY;
+    return;
+  }
+  double l = 0.0;
+  for (long j = 0; j < n; ++j) {
+    if (!is_visible(i, j, Sq, n, causal, ks, ke)) continue;
+    double e = exp(s[j] - m);
+    l += e;
+    for (long c = 0; c < d; ++c) u[c] += e * ld(v, vbase + j * d + c);
+  }
+  *m_out = m;
+  *l_out = l;
+  for (long c = 0; c < d; ++c) o[c] = u[c] / l;
+  *lse_out = m + log(l);
+}
+
+/*
+ * Single-row state (m, l, u, O, LSE) for one query against n keys, all
+ * inputs fp64, no mask beyond the optional causal rule for row i of Sq.
+ */
+int oracle_row_state(const double* q, const double* k, const double* v, long n, long d,
+                     double scale, double* m, double* l, double* u, double* o, double* lse) {
+  double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  if (!s) return 1;
+  src_t ks = {k, 0}, vs = {v, 0};
+  row_attention(q, ks, 0, vs, 0, n, d, scale, 0, 1, 0, 0, n, s, m, l, u, o, lse);
+  free(s);
+  return 0;
+}
+
+/*
+ * Forward over [B, Hq, Sq, d] queries.  rows == NULL computes every row and
+ * writes o[B*Hq*Sq*d], lse[B*Hq*Sq]; otherwise rows holds nrows flat row ids
+ * ((b*Hq + h)*Sq + i) and o/lse are packed in that order.  m_out/l_out are
+ * optional and follow the same packing.
+ */
+int oracle_fwd(const void* q, const void* k, const void* v, int in_bf16, long B, long Hq,
+               long Hkv, long Sq, long Sk, long d, int causal, double scale,
+               const int* k_start, const int* k_end, long nrows, const long* rows,
+               double* o, double* lse, double* m_out, double* l_out) {
+  if (Hkv <= 0 || Hq % Hkv != 0) return 1;
+  const long group = Hq / Hkv;
+  const long total = rows ? nrows : B * Hq * Sq;
+  src_t qs = {q, in_bf16}, kk = {k, in_bf16}, vv = {v, in_bf16};
+  int err = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+    double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+    double* u = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!s || !qrow || !u) {
+#pragma omp atomic write
+      err = 1;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (long r = 0; r < total; ++r) {
+        const long flat = rows ? rows[r] : r;
+        const long i = flat % Sq;
+        const long h = (flat / Sq) % Hq;
+        const long b = flat / (Sq * Hq);
+        const long hk = h / group;
+        long ks, ke;
+        key_range(k_start, k_end, b, Sk, &ks, &ke);
+        load_row(qs, flat * d, d, qrow);
+        const long kvbase = (b * Hkv + hk) * Sk * d;
+        double m, l;
+        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, s,
+                      &m, &l, u, o + r * d, lse + r);
+        if (m_out) m_out[r] = m;
+        if (l_out) l_out[r] = l;
+      }
+    }
+    free(s);
+    free(qrow);
+    free(u);
+  }
+  return err;
+}
+
+/*
+ * Dense probabilities and score gradients for small problems:
+ * p[B,Hq,Sq,Sk] and ds[B,Hq,Sq,Sk] (ds may be NULL, dout then unused).
+ */
+int oracle_probs(const void* q, const void* k, const void* v, const void* dout, int in_bf16,
+                 long B, long Hq, long Hkv, long Sq, long Sk, long d, int causal,
+                 double scale, const int* k_start, const int* k_end, double* p, double* ds) {
+  if (Hkv <= 0 || Hq % Hkv != 0) return 1;
+  const long group = Hq / Hkv;
+  src_t qs = {q, in_bf16}, kk = {k, in_bf16}, vv = {v, in_bf16}, dos = {dout, in_bf16};
+  double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+  double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+  double* u = (double*)malloc(sizeof(double) * (size_t)d);
+  double* orow = (double*)malloc(sizeof(double) * (size_t)d);
+  if (!s || !qrow || !u || !orow) return 1;
+  for (long b = 0; b < B; ++b)
+    for (long h = 0; h < Hq; ++h)
+      for (long i = 0; i < Sq; ++i) {
+        const long flat = (b * Hq + h) * Sq + i;
+        const long kvbase = (b * Hkv + h / group) * Sk * d;
+        long ks, ke;
+        key_range(k_start, k_end, b, Sk, &ks, &ke);
+        load_row(qs, flat * d, d, qrow);
+        double m, l, lse;
+        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, s, &m,
+                      &l, u, orow, &lse);
+        double D = 0.0;
+        if (ds)
+          for (long c = 0; c < d; ++c) D += ld(dos, flat * d + c) * orow[c];
+        for (long j = 0; j < Sk; ++j) {
+          const long idx = flat * Sk + j;
+          double pij = 0.0;
+          if (l > 0.0 && is_visible(i, j, Sq, Sk, causal, ks, ke)) pij = exp(s[j] - m) / l;
+          p[idx] = pij;
+          if (ds) {
+            double dp = 0.0;
+            for (long c = 0; c < d; ++c) dp += ld(dos, flat * d + c) * ld(vv, kvbase + j * d + c);
+            ds[idx] = pij * (dp - D);
+          }
+        }
+      }
+  free(s);
+  free(qrow);
+  free(u);
+  free(orow);
+  return 0;
+}
+
+/*
+ * Full backward: dq[B,Hq,Sq,d], dk/dv[B,Hkv,Sk,d], all fp64.
+ * Per-row statistics m_i, l_i and D_i are formed first from the definition;
+ * every p_ij and dS_ij is then evaluated from them where it is needed.
+ */
+int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, int in_bf16,
+               long B, long Hq, long Hkv, long Sq, long Sk, long d, int causal, double scale,
+               const int* k_start, const int* k_end, double* dq, double* dk, double* dv) {
+  if (Hkv <= 0 || Hq % Hkv != 0) return 1;
+  const long group = Hq / Hkv;
+  const long nrow = B * Hq * Sq;
+  src_t qs = {q, in_bf16}, kk = {k, in_bf16}, vv = {v, in_bf16}, dos = {dout, in_bf16};
+  double* M = (double*)malloc(sizeof(double) * (size_t)(nrow > 0 ? nrow : 1));
+  double* L = (double*)malloc(sizeof(double) * (size_t)(nrow > 0 ? nrow : 1));
+  double* Dv = (double*)malloc(sizeof(double) * (size_t)(nrow > 0 ? nrow : 1));
+  if (!M || !L || !Dv) return 1;
+  int err = 0;
+
+  /* pass 1: row statistics m_i, l_i, D_i = <dO_i, O_i>, and dQ_i */
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+    double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+    double* dorow = (double*)malloc(sizeof(double) * (size_t)d);
+    double* u = (double*)malloc(sizeof(double) * (size_t)d);
+    double* orow = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!s || !qrow || !dorow || !u || !orow) {
+#pragma omp atomic write
+      err = 1;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (long flat = 0; flat < nrow; ++flat) {
+        const long i = flat % Sq;
+        const long h = (flat / Sq) % Hq;
+        const long b = flat / (Sq * Hq);
+        const long kvbase = (b * Hkv + h / group) * Sk * d;
+        long ks, ke;
+        key_range(k_start, k_end, b, Sk, &ks, &ke);
+        load_row(qs, flat * d, d, qrow);
+        load_row(dos, flat * d, d, dorow);
+        double lse;
+        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, s,
+                      &M[flat], &L[flat], u, orow, &lse);
+        double D = 0.0;
+        for (long c = 0; c < d; ++c) D += dorow[c] * orow[c];
+        Dv[flat] = D;
+        double* dqr = dq + flat * d;
+        for (long c = 0; c < d; ++c) dqr[c] = 0.0;
+        if (L[flat] <= 0.0) continue;
+        for (long j = 0; j < Sk; ++j) {
+          if (!is_visible(i, j, Sq, Sk, causal, ks, ke)) continue;
+          const double pij = exp(s[j] - M[flat]) / L[flat];
+          double dp = 0.0;
+          for (long c = 0; c < d; ++c) dp += dorow[c] * ld(vv, kvbase + j * d + c);
+          const double dsij = pij * (dp - D);
+          for (long c = 0; c < d; ++c) dqr[c] += scale * dsij * ld(kk, kvbase + j * d + c);
+        }
+      }
+    }
+    free(s);
+    free(qrow);
+    free(dorow);
+    free(u);
+    free(orow);
+  }
+  if (err) goto done;
+
+  /* pass 2: dK_j and dV_j, summing over every query row of every query head
+     in the group that reads KV head hk */
+#pragma omp parallel
+  {
+    double* krow = (double*)malloc(sizeof(double) * (size_t)d);
+    double* vrow = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!krow || !vrow) {
+#pragma omp atomic write
+      err = 1;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (long flatk = 0; flatk < B * Hkv * Sk; ++flatk) {
+        const long j = flatk % Sk;
+        const long hk = (flatk / Sk) % Hkv;
+        const long b = flatk / (Sk * Hkv);
+        long ks, ke;
+        key_range(k_start, k_end, b, Sk, &ks, &ke);
+        load_row(kk, flatk * d, d, krow);
+        load_row(vv, flatk * d, d, vrow);
+        double* dkr = dk + flatk * d;
+        double* dvr = dv + flatk * d;
+        for (long c = 0; c < d; ++c) dkr[c] = dvr[c] = 0.0;
+        for (long g = 0; g < group; ++g) {
+          const long h = hk * group + g;
+          for (long i = 0; i < Sq; ++i) {
+            if (!is_visible(i, j, Sq, Sk, causal, ks, ke)) continue;
+            const long flat = (b * Hq + h) * Sq + i;
+            if (L[flat] <= 0.0) continue;
+            double sij = 0.0, dp = 0.0;
+            for (long c = 0; c < d; ++c) sij += ld(qs, flat * d + c) * krow[c];
+            sij *= scale;
+            for (long c = 0; c < d; ++c) dp += ld(dos, flat * d + c) * vrow[c];
+            const double pij = exp(sij - M[flat]) / L[flat];
+            const double dsij = pij * (dp - Dv[flat]);
+            for (long c = 0; c < d; ++c) {
+              dvr[c] += pij * ld(dos, flat * d + c);
+              dkr[c] += scale * dsij * ld(qs, flat * d + c);
+            }
+          }
+        }
+      }
+    }
+    free(krow);
+    free(vrow);
+  }
+done:
+  free(M);
+  free(L);
+  free(Dv);
+  return err;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

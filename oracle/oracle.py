@@ -1,0 +1,211 @@
+"""FP64 CPU oracle for exact scaled-dot-product attention (ctypes binding).
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers.  The product path never
+imports this module, and this module never imports the product package.
+
+The arithmetic lives in ``fa_oracle.c`` (plain definition, no tiling); this file
+only compiles it with gcc, marshals arrays and returns fp64 numpy results.
+Every function below states which passage of the pages it follows.
+
+Parity pins (see tests/test_oracle.py): the worked example of the
+FlashAttention_01 page ("large scores" practice section), tiled-vs-untiled
+agreement against ``online_softmax.py``, torch fp64 CPU SDPA and its autograd,
+central differences, and the gradient invariants of the chain-rule section.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile fa_oracle.c into liboracle.so (gcc, OpenMP, no -march flags)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            L = ctypes.c_long
+            lib.oracle_fwd.argtypes = [P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
+                                       ctypes.c_double, P, P, L, P, P, P, P, P]
+            lib.oracle_bwd.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
+                                       ctypes.c_double, P, P, P, P, P]
+            lib.oracle_probs.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
+                                         ctypes.c_double, P, P, P, P]
+            lib.oracle_row_state.argtypes = [P, P, P, L, L, ctypes.c_double, P, P, P, P, P]
+            for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_probs, lib.oracle_row_state):
+                f.restype = ctypes.c_int
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _as_input(x):
+    """Return (contiguous numpy array, is_bf16).  bf16 torch tensors are passed
+    as their raw bit patterns; the C side widens them to fp64 exactly."""
+    try:
+        import torch  # local: the oracle itself does not depend on torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16), 1
+            return x.to(torch.float64).numpy(), 0
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(x)
+    if a.dtype == np.uint16:
+        return a, 1
+    return np.ascontiguousarray(a, dtype=np.float64), 0
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _i32(x, B):
+    if x is None:
+        return None
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+    assert a.shape == (B,)
+    return a
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, rows=None,
+        return_stats: bool = False):
+    """Forward O and LSE from the definition (the "Flash Attention" history page
+    1.1-1.2; FlashAttention_01 page, online-softmax derivation, masking rule).
+
+    q: [B,Hq,Sq,d], k/v: [B,Hkv,Sk,d] (bf16 torch tensors or float arrays).
+    rows: optional flat row ids ((b*Hq+h)*Sq+i); results are then packed
+    [len(rows), d] / [len(rows)].  Fully masked rows give O=0, LSE=-inf.
+    """
+    qa, bf = _as_input(q)
+    ka, bk = _as_input(k)
+    va, bv = _as_input(v)
+    assert bf == bk == bv, "q, k, v must share one input type"
+    B, Hq, Sq, d = qa.shape
+    _, Hkv, Sk, _ = ka.shape
+    ks = _i32(k_start, B)
+    ke = _i32(k_end, B)
+    if rows is None:
+        n = B * Hq * Sq
+        rr = None
+    else:
+        rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = rr.shape[0]
+    o = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    m = np.empty((n,), np.float64) if return_stats else None
+    l = np.empty((n,), np.float64) if return_stats else None
+    rc = _load().oracle_fwd(_ptr(qa), _ptr(ka), _ptr(va), bf, B, Hq, Hkv, Sq, Sk, d, int(causal),
+                            float(scale), _ptr(ks), _ptr(ke), n, _ptr(rr), _ptr(o), _ptr(lse),
+                            _ptr(m), _ptr(l))
+    if rc:
+        raise RuntimeError(f"oracle_fwd failed ({rc})")
+    if rows is None:
+        o = o.reshape(B, Hq, Sq, d)
+        lse = lse.reshape(B, Hq, Sq)
+        if return_stats:
+            m = m.reshape(B, Hq, Sq)
+            l = l.reshape(B, Hq, Sq)
+    if return_stats:
+        return o, lse, m, l
+    return o, lse
+
+
+def bwd(q, k, v, dout, causal: bool, scale: float, k_start=None, k_end=None):
+    """dQ, dK, dV from the definition (FlashAttention_01 page, "why the backward
+    can recompute" and the chain-rule section): dV=P^T dO, dP=dO V^T,
+    dS=P*(dP-rowsum(dO*O)), dQ=scale dS K, dK=scale dS^T Q; GQA heads summed."""
+    qa, bf = _as_input(q)
+    ka, _ = _as_input(k)
+    va, _ = _as_input(v)
+    da, _ = _as_input(dout)
+    B, Hq, Sq, d = qa.shape
+    _, Hkv, Sk, _ = ka.shape
+    dq = np.empty((B, Hq, Sq, d), np.float64)
+    dk = np.empty((B, Hkv, Sk, d), np.float64)
+    dv = np.empty((B, Hkv, Sk, d), np.float64)
+    rc = _load().oracle_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), bf, B, Hq, Hkv, Sq, Sk, d,
+                            int(causal), float(scale), _ptr(_i32(k_start, B)),
+                            _ptr(_i32(k_end, B)), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc:
+        raise RuntimeError(f"oracle_bwd failed ({rc})")
+    return dq, dk, dv
+
+
+def probs(q, k, v, causal: bool, scale: float, dout=None, k_start=None, k_end=None):
+    """Dense P [B,Hq,Sq,Sk] and, when dout is given, dS (small problems only)."""
+    qa, bf = _as_input(q)
+    ka, _ = _as_input(k)
+    va, _ = _as_input(v)
+    da = _as_input(dout)[0] if dout is not None else None
+    B, Hq, Sq, d = qa.shape
+    _, Hkv, Sk, _ = ka.shape
+    p = np.empty((B, Hq, Sq, Sk), np.float64)
+    ds = np.empty((B, Hq, Sq, Sk), np.float64) if dout is not None else None
+    rc = _load().oracle_probs(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), bf, B, Hq, Hkv, Sq, Sk, d,
+                              int(causal), float(scale), _ptr(_i32(k_start, B)),
+                              _ptr(_i32(k_end, B)), _ptr(p), _ptr(ds))
+    if rc:
+        raise RuntimeError(f"oracle_probs failed ({rc})")
+    return (p, ds) if dout is not None else p
+
+
+def row_state(q, k, v, scale: float):
+    """(m, l, u, O, LSE) of one query q[d] over keys k[n,d], values v[n,d],
+    fp64, all keys visible (FlashAttention_01 page, worked example)."""
+    qa = np.ascontiguousarray(q, dtype=np.float64)
+    ka = np.ascontiguousarray(k, dtype=np.float64)
+    va = np.ascontiguousarray(v, dtype=np.float64)
+    n, d = ka.shape
+    m = np.zeros(1)
+    l = np.zeros(1)
+    lse = np.zeros(1)
+    u = np.zeros(d)
+    o = np.zeros(d)
+    rc = _load().oracle_row_state(_ptr(qa), _ptr(ka), _ptr(va), n, d, float(scale), _ptr(m),
+                                  _ptr(l), _ptr(u), _ptr(o), _ptr(lse))
+    if rc:
+        raise RuntimeError("oracle_row_state failed")
+    return float(m[0]), float(l[0]), u, o, float(lse[0])
+
+
+def decode(q, k_cache, v_cache, seqlens_k, scale: float, rows=None):
+    """Sq=1 decode = the forward with Sq=1 and key interval [0, seqlens_k[b])
+    (FlashAttention_01 page, prefill/decode timed separately); no split."""
+    B = q.shape[0]
+    return fwd(q, k_cache, v_cache, causal=False, scale=scale, k_start=None,
+               k_end=_i32(seqlens_k, B), rows=rows)

@@ -1,0 +1,343 @@
+"""Pins of the FP64 oracle against what the pages and the mathematics fix.
+
+Each test names the passage it follows.  None of these values comes from the
+CUDA path: they are the pages' printed numbers, closed forms, brute force or a
+library routine (torch fp64 CPU SDPA and its autograd) the oracle does not use.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from oracle import online_softmax as ons
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rand(shape, seed, dtype=torch.float64, mult=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g, dtype=torch.float64) * mult).to(dtype)
+
+
+# --- worked example (FlashAttention_01 page, large-score practice section) ---
+
+def test_worked_example_printed_values():
+    g = _golden("worked_example.json")
+    k = np.array(g["scores"])[:, None]
+    v = np.array(g["values"])[:, None]
+    m, l, u, o, lse = orc.row_state(np.array([1.0]), k, v, scale=1.0)
+    tol = 0.5 * 10.0 ** (-g["printed_decimals"]) + 1e-12
+    last = g["printed_steps"][-1]
+    assert m == last["m"]
+    assert abs(l - last["l"]) <= tol
+    assert abs(u[0] - last["u"]) <= tol
+    assert abs(o[0] - g["printed_output"]) <= tol
+    assert math.isfinite(lse)
+
+
+def test_worked_example_closed_form():
+    k = np.array([[1000.0], [1001.0], [999.0]])
+    v = np.array([[1.0], [3.0], [7.0]])
+    m, l, u, o, lse = orc.row_state(np.array([1.0]), k, v, scale=1.0)
+    e1, e2 = math.exp(-1.0), math.exp(-2.0)
+    assert abs(l - (e1 + 1.0 + e2)) < 1e-14
+    assert abs(u[0] - (e1 * 1 + 3 + 7 * e2)) < 1e-13
+    assert abs(o[0] - (e1 + 3 + 7 * e2) / (e1 + 1 + e2)) < 1e-14
+    assert abs(lse - (1001.0 + math.log(e1 + 1 + e2))) < 1e-12
+
+
+def test_worked_example_step_trace():
+    """One key per tile: the recurrence's states after each block are the
+    printed (m, l, u) triples."""
+    g = _golden("worked_example.json")
+    trace = []
+    ons.tiled_row([1.0], np.array(g["scores"])[:, None], np.array(g["values"])[:, None],
+                  tile=1, scale=1.0, trace=trace)
+    tol = 0.5 * 10.0 ** (-g["printed_decimals"]) + 1e-12
+    for (m, l, u), want in zip(trace, g["printed_steps"]):
+        assert m == want["m"]
+        assert abs(l - want["l"]) <= tol
+        assert abs(u[0] - want["u"]) <= tol
+
+
+def test_worked_example_bf16_encoding_is_exact():
+    """The bf16 encoding used on the GPU reproduces scores 1000, 1001, 999."""
+    from io_aware_exact_tcgen05_gb300.workloads import worked_example_bf16
+    q, k, v = worked_example_bf16()
+    s = (k.double()[0, 0] @ q.double()[0, 0, 0])
+    assert s.tolist() == [1000.0, 1001.0, 999.0]
+    assert v.double()[0, 0, :, 0].tolist() == [1.0, 3.0, 7.0]
+    o, lse = orc.fwd(q, k, v, causal=False, scale=1.0)
+    e1, e2 = math.exp(-1.0), math.exp(-2.0)
+    assert abs(o[0, 0, 0, 0] - (e1 + 3 + 7 * e2) / (e1 + 1 + e2)) < 1e-14
+    assert np.all(o[0, 0, 0, 1:] == 0.0)
+
+
+# --- tiled vs one-shot (FlashAttention_01 page, reviewable experiment) ---
+
+@pytest.mark.parametrize("tile", [1, 2, 3, 8, 16, 37])
+@pytest.mark.parametrize("mult", [1.0, 300.0])
+def test_tiled_recurrence_matches_untiled_oracle(tile, mult):
+    n, d = 100, 16  # 100 keys: every listed tile length leaves a ragged last block
+    q = _rand((d,), 1, mult=mult).numpy()
+    K = _rand((n, d), 2).numpy()
+    V = _rand((n, d), 3).numpy()
+    m1, l1, u1, o1, lse1 = ons.tiled_row(q, K, V, tile)
+    m0, l0, u0, o0, lse0 = orc.row_state(q, K, V, 1.0 / math.sqrt(d))
+    assert np.all(np.isfinite(o1)) and math.isfinite(lse1)
+    scale_o = max(1.0, float(np.abs(o0).max()))
+    assert float(np.abs(o1 - o0).max()) <= 1e-12 * scale_o
+    assert abs(lse1 - lse0) <= 1e-12 * max(1.0, abs(lse0))
+    assert abs(m1 - m0) <= 1e-14 * max(1.0, abs(m0))  # dot-product order differs
+
+
+def test_tiled_recurrence_with_mask_and_empty_row():
+    n, d = 37, 8
+    q = _rand((d,), 4).numpy()
+    K = _rand((n, d), 5).numpy()
+    V = _rand((n, d), 6).numpy()
+    vis = np.zeros(n, bool)
+    vis[10:20] = True
+    for tile in (1, 2, 3, 8):
+        m, l, u, o, lse = ons.tiled_row(q, K, V, tile, visible=vis)
+        _, _, _, o0, lse0 = orc.row_state(q, K[10:20], V[10:20], 1.0 / math.sqrt(d))
+        assert np.abs(o - o0).max() < 1e-13 and abs(lse - lse0) < 1e-13
+    m, l, u, o, lse = ons.tiled_row(q, K, V, 3, visible=np.zeros(n, bool))
+    assert m == -np.inf and l == 0.0 and lse == -np.inf and np.all(o == 0)
+
+
+# --- cross-check with the framework's native SDPA, fp64 CPU (FlashAttention_01
+#     page, 5.1: build the numerical baseline with native SDPA) ---
+
+def _mask(Sq, Sk, causal, ks, ke, B):
+    i = torch.arange(Sq)[:, None]
+    j = torch.arange(Sk)[None, :]
+    m = torch.ones(B, 1, Sq, Sk, dtype=torch.bool)
+    for b in range(B):
+        vis = (j >= ks[b]) & (j < ke[b])
+        if causal:
+            vis = vis & (j <= i + Sk - Sq)
+        m[b, 0] = vis
+    return m
+
+
+CASES = [
+    # B, Hq, Hkv, Sq, Sk, d, causal, ks, ke
+    (2, 4, 4, 33, 33, 16, True, None, None),
+    (1, 4, 2, 17, 29, 8, True, None, None),
+    (2, 6, 2, 31, 20, 16, False, [3, 0], [20, 11]),
+    (2, 4, 1, 24, 24, 32, True, [5, 0], [24, 24]),
+    (1, 2, 2, 1, 40, 8, False, [0], [13]),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_forward_matches_torch_sdpa_fp64(case):
+    B, Hq, Hkv, Sq, Sk, d, causal, ks, ke = case
+    ks = ks or [0] * B
+    ke = ke or [Sk] * B
+    q = _rand((B, Hq, Sq, d), 10)
+    k = _rand((B, Hkv, Sk, d), 11)
+    v = _rand((B, Hkv, Sk, d), 12)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = orc.fwd(q, k, v, causal, scale, k_start=ks, k_end=ke)
+    mask = _mask(Sq, Sk, causal, ks, ke, B)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q, k, v, attn_mask=mask, scale=scale, enable_gqa=(Hq != Hkv))
+    rep = Hq // Hkv
+    s = torch.einsum("bhid,bhjd->bhij", q, k.repeat_interleave(rep, 1)) * scale
+    s = s.masked_fill(~mask, -math.inf)
+    ref_lse = torch.logsumexp(s, -1)
+    live = mask.any(-1).expand(B, Hq, Sq)
+    assert np.abs(o[live.numpy()] - ref[live].numpy()).max() < 1e-12
+    assert np.abs(lse[live.numpy()] - ref_lse[live].numpy()).max() < 1e-12
+    dead = ~live.numpy()
+    assert np.all(o[dead] == 0.0) and np.all(lse[dead] == -np.inf)
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_backward_matches_torch_autograd_fp64(case):
+    B, Hq, Hkv, Sq, Sk, d, causal, ks, ke = case
+    ks = ks or [0] * B
+    ke = ke or [Sk] * B
+    q = _rand((B, Hq, Sq, d), 20)
+    k = _rand((B, Hkv, Sk, d), 21)
+    v = _rand((B, Hkv, Sk, d), 22)
+    do = _rand((B, Hq, Sq, d), 23)
+    scale = 1.0 / math.sqrt(d)
+    mask = _mask(Sq, Sk, causal, ks, ke, B)
+    live = mask.any(-1).expand(B, Hq, Sq)
+    # torch yields NaN rows where nothing is visible; zero their upstream grad
+    do_t = do.masked_fill(~live[..., None], 0.0)
+    qt, kt, vt = (x.clone().requires_grad_() for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt, vt, attn_mask=mask, scale=scale, enable_gqa=(Hq != Hkv))
+    ref = torch.where(live[..., None], ref, torch.zeros_like(ref))
+    ref.backward(do_t)
+    dq, dk, dv = orc.bwd(q, k, v, do, causal, scale, k_start=ks, k_end=ke)
+    for mine, theirs in ((dq, qt.grad), (dk, kt.grad), (dv, vt.grad)):
+        assert np.abs(mine - theirs.numpy()).max() < 1e-11
+    assert np.all(dq[~live.numpy()] == 0.0)
+
+
+# --- chain-rule section: central differences on the 2x3x2 masked example ---
+
+def _loss(q, k, v):
+    o, _ = orc.fwd(q, k, v, causal=True, scale=1.0 / math.sqrt(2))
+    return 0.5 * float((o ** 2).sum())
+
+
+def test_central_differences_2x3_masked():
+    """2 queries, 3 keys, d=2; row 0 may not read key 2 (bottom-right causal
+    rule, Sq=2, Sk=3); J = 0.5*sum(O^2) so dO = O."""
+    q = _rand((1, 1, 2, 2), 30).numpy()
+    k = _rand((1, 1, 3, 2), 31).numpy()
+    v = _rand((1, 1, 3, 2), 32).numpy()
+    p = orc.probs(q, k, v, causal=True, scale=1.0 / math.sqrt(2))
+    assert p[0, 0, 0, 2] == 0.0 and p[0, 0, 1, 2] > 0.0
+    o, _ = orc.fwd(q, k, v, causal=True, scale=1.0 / math.sqrt(2))
+    dq, dk, dv = orc.bwd(q, k, v, o, causal=True, scale=1.0 / math.sqrt(2))
+    h = 1e-6
+    worst = 0.0
+    for arr, grad in ((q, dq), (k, dk), (v, dv)):
+        for idx in np.ndindex(arr.shape):
+            save = arr[idx]
+            arr[idx] = save + h
+            jp = _loss(q, k, v)
+            arr[idx] = save - h
+            jm = _loss(q, k, v)
+            arr[idx] = save
+            num = (jp - jm) / (2 * h)
+            worst = max(worst, abs(num - grad[idx]))
+    assert worst < 1e-8, worst
+
+
+# --- gradient invariants (chain-rule section) ---
+
+def test_gradient_invariants():
+    B, Hq, Hkv, Sq, Sk, d = 2, 4, 2, 12, 12, 8
+    ks, ke = [4, 0], [12, 9]
+    q, k, v, do = (_rand(s, 40 + i) for i, s in enumerate(
+        [(B, Hq, Sq, d), (B, Hkv, Sk, d), (B, Hkv, Sk, d), (B, Hq, Sq, d)]))
+    scale = 1.0 / math.sqrt(d)
+    p, ds = orc.probs(q, k, v, causal=True, scale=scale, dout=do, k_start=ks, k_end=ke)
+    mask = _mask(Sq, Sk, True, ks, ke, B).expand(B, Hq, Sq, Sk).numpy()
+    assert np.abs(ds.sum(-1)).max() < 1e-13  # rowsum dS = 0
+    assert np.all(p[~mask] == 0.0) and np.all(ds[~mask] == 0.0)
+    live = mask.any(-1)
+    assert np.allclose(p.sum(-1)[live], 1.0, atol=1e-14)
+    dq, dk, dv = orc.bwd(q, k, v, do, True, scale, k_start=ks, k_end=ke)
+    assert np.abs(dk.sum(2)).max() < 1e-12  # sum_j dK_j = 0 per (b, hkv)
+    # sum_j dV_j = sum over non-empty rows of dO, per KV head
+    dos = do.numpy() * live[..., None]
+    want = dos.reshape(B, Hkv, Hq // Hkv, Sq, d).sum((2, 3))
+    assert np.abs(dv.sum(2) - want).max() < 1e-12
+
+
+# --- special cases (boundary section: single visible key, empty row, repeated maxima) ---
+
+def test_single_visible_key():
+    q = _rand((1, 1, 1, 4), 50)
+    k = _rand((1, 1, 6, 4), 51)
+    v = _rand((1, 1, 6, 4), 52)
+    o, lse = orc.fwd(q, k, v, False, 0.5, k_start=[3], k_end=[4])
+    assert np.abs(o[0, 0, 0] - v[0, 0, 3].numpy()).max() == 0.0
+    assert abs(lse[0, 0, 0] - 0.5 * float(q[0, 0, 0] @ k[0, 0, 3])) < 1e-15
+
+
+def test_zero_query_gives_mean_and_log_count():
+    q = torch.zeros(1, 1, 5, 8, dtype=torch.float64)
+    k = _rand((1, 1, 5, 8), 53)
+    v = _rand((1, 1, 5, 8), 54)
+    o, lse = orc.fwd(q, k, v, True, 0.3)
+    for i in range(5):
+        assert np.abs(o[0, 0, i] - v[0, 0, : i + 1].numpy().mean(0)).max() < 1e-15
+        assert abs(lse[0, 0, i] - math.log(i + 1)) < 1e-15
+
+
+def test_fully_masked_rows_are_zero_and_finite():
+    B, H, S, d = 1, 2, 10, 8
+    q, k, v, do = (_rand((B, H, S, d), 60 + i) for i in range(4))
+    o, lse = orc.fwd(q, k, v, True, 0.25, k_start=[4], k_end=[10])
+    assert np.all(o[0, :, :4] == 0.0) and np.all(lse[0, :, :4] == -np.inf)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse[0, :, 4:]))
+    dq, dk, dv = orc.bwd(q, k, v, do, True, 0.25, k_start=[4], k_end=[10])
+    for g in (dq, dk, dv):
+        assert np.all(np.isfinite(g))
+    assert np.all(dq[0, :, :4] == 0.0)
+    assert np.all(dk[0, :, :4] == 0.0) and np.all(dv[0, :, :4] == 0.0)
+
+
+def test_repeated_maxima():
+    K = np.array([[2.0], [2.0], [1.0], [2.0]])
+    V = np.array([[1.0], [2.0], [3.0], [4.0]])
+    m, l, u, o, lse = orc.row_state(np.array([1.0]), K, V, 1.0)
+    e = math.exp(-1.0)
+    assert m == 2.0
+    assert abs(l - (3 + e)) < 1e-15
+    assert abs(o[0] - (1 + 2 + 4 + 3 * e) / (3 + e)) < 1e-15
+    for tile in (1, 2, 3):
+        _, _, _, ot, _ = ons.tiled_row([1.0], K, V, tile, scale=1.0)
+        assert abs(ot[0] - o[0]) < 1e-15
+
+
+def test_large_logits_stay_finite():
+    q = _rand((1, 2, 16, 8), 70, mult=800.0)
+    k = _rand((1, 2, 16, 8), 71)
+    v = _rand((1, 2, 16, 8), 72)
+    o, lse = orc.fwd(q, k, v, True, 1.0)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    assert np.abs(lse).max() > 710  # exp(lse) itself would overflow fp64
+
+
+# --- decode and split-KV merge ---
+
+def test_decode_equals_forward_with_interval_and_split_invariance():
+    B, Hq, Hkv, Smax, d = 3, 4, 2, 50, 8
+    q = _rand((B, Hq, 1, d), 80)
+    k = _rand((B, Hkv, Smax, d), 81)
+    v = _rand((B, Hkv, Smax, d), 82)
+    lens = [50, 7, 23]
+    o, lse = orc.decode(q, k, v, lens, 0.35)
+    o2, lse2 = orc.fwd(q, k, v, False, 0.35, k_start=[0] * B, k_end=lens)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    for b in range(B):
+        for h in range(Hq):
+            for chunk in (1, 5, 16, 64):
+                states = []
+                for c0 in range(0, Smax, chunk):
+                    oc, lc = orc.fwd(q[b:b + 1], k[b:b + 1], v[b:b + 1], False, 0.35,
+                                     k_start=[c0], k_end=[min(c0 + chunk, lens[b])])
+                    states.append((lc[0, h, 0], oc[0, h, 0]))
+                lm, om = ons.merge_states(states)
+                assert abs(lm - lse[b, h, 0]) < 1e-12
+                assert np.abs(om - o[b, h, 0]).max() < 1e-12
+
+
+def test_bf16_inputs_widen_exactly():
+    q = _rand((1, 2, 9, 16), 90).to(torch.bfloat16)
+    k = _rand((1, 1, 9, 16), 91).to(torch.bfloat16)
+    v = _rand((1, 1, 9, 16), 92).to(torch.bfloat16)
+    a = orc.fwd(q, k, v, True, 0.25)
+    b = orc.fwd(q.double(), k.double(), v.double(), True, 0.25)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_row_subset_equals_full():
+    q = _rand((2, 4, 20, 8), 95)
+    k = _rand((2, 2, 20, 8), 96)
+    v = _rand((2, 2, 20, 8), 97)
+    o, lse = orc.fwd(q, k, v, True, 0.3, k_start=[2, 0], k_end=[20, 15])
+    rows = [0, 1, 5, 79, 80, 159]
+    os_, ls = orc.fwd(q, k, v, True, 0.3, k_start=[2, 0], k_end=[20, 15], rows=rows)
+    assert np.array_equal(os_, o.reshape(-1, 8)[rows])
+    assert np.array_equal(ls, lse.reshape(-1)[rows])
