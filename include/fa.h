@@ -1,0 +1,146 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact scaled-dot-product attention on GB300
+ * (sm_103a), computed tile by tile with the online-softmax recurrence.
+ *
+ * What every call computes (the pages' definition; the kernels never write an
+ * S x S matrix to device memory):
+ *
+ *   S = scale * Q K^T,  P = softmax(S) over the visible keys of each row,
+ *   O = P V,  LSE_i = ln sum_j exp(S_ij)  (natural log, scale included)
+ *
+ *   -- "Flash Attention" history page, sections 1.1 (the attention formula),
+ *      1.2 (running max m, denominator l, rescaled output), 1.3 (tiles live on
+ *      chip and are discarded), 2.1 (parallelism over the query sequence,
+ *      causal tiles skipped); FlashAttention_01 page, "online softmax
+ *      derivation" (m, l, unnormalised u, divide once at the end; mask before
+ *      the max; an explicit rule for rows with no visible key) and "backward
+ *      recomputation" (save one logsumexp per row, rebuild P from it).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  * Tensors are bf16 (IEEE bfloat16 bit patterns), contiguous, layout
+ *    [B, H, S, d] with d innermost.  Q, O, dO, dQ: [B, Hq, Sq, d].
+ *    K, V, dK, dV: [B, Hkv, Sk, d].  LSE: fp32 [B, Hq, Sq].
+ *  * Every pointer is a DEVICE pointer of the current CUDA device, 16-byte
+ *    aligned.  The caller owns every buffer and the stream; the library never
+ *    allocates, frees or retains device memory (scratch comes from the
+ *    caller's workspace argument).
+ *  * Grouped K/V heads (GQA/MQA, "Flash Attention" practitioner page 2.3):
+ *    Hq % Hkv == 0 and query head h reads KV head h / (Hq / Hkv).
+ *  * Visibility of key j to query row i of batch row b:
+ *        k_start[b] <= j < k_end[b]   and   (causal == 0  or  j <= i + Sk - Sq)
+ *    The causal rule is aligned to the bottom-right corner (for Sq == Sk it is
+ *    the usual lower triangle).  k_start / k_end are optional device int32[B]
+ *    arrays (NULL means 0 and Sk); values outside [0, Sk] are clamped.
+ *  * A row with no visible key gets O = 0 and LSE = -inf, and contributes zero
+ *    gradient; no -inf - (-inf) is ever evaluated.
+ *  * d (head dimension) must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
+ *  * Calls are asynchronous: they validate, enqueue kernels on `stream` and
+ *    return.  A validation failure returns before any launch and writes
+ *    nothing.  Launch failures return FA_ERR_CUDA.  fa_last_error_detail()
+ *    gives a one-line reason for the last non-OK status of the calling thread.
+ *  * Device-side pipeline waits are bounded (1 s).  A wait that runs out
+ *    records FA_ERR_TIMEOUT in a device status word and the kernel returns
+ *    early; fa_device_status() reads (and optionally clears) that word.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* bad size, null or misaligned pointer, Hq % Hkv != 0 */
+  FA_ERR_UNSUPPORTED = 2, /* head dimension other than 64 or 128, or no sm_103a device */
+  FA_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than the *_workspace_size query */
+  FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  FA_ERR_TIMEOUT = 5      /* a device pipeline wait ran out (see fa_device_status) */
+} fa_status;
+
+/*
+ * Forward pass.  O = softmax(scale * Q K^T) V over visible keys, and per-row
+ * LSE (natural log, scale included).  lse may be NULL when the caller does
+ * not need it; the backward needs it.
+ *   q [B,Hq,Sq,d], k/v [B,Hkv,Sk,d], o [B,Hq,Sq,d] (written), lse [B,Hq,Sq]
+ *   (written).  B, Hq, Hkv, Sq, Sk >= 1.
+ * Follows: "Flash Attention" history page 1.2-1.3 and 2.1; FlashAttention_01
+ * page, online-softmax derivation and the large-score worked example.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                 int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                 const int32_t* k_start, const int32_t* k_end, cudaStream_t stream);
+
+/* Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator
+   [B,Hq,Sq,d] and the fp32 row terms D_i = rowsum(dO * O) [B,Hq,Sq]. */
+size_t fa_bwd_workspace_size(int B, int Hq, int Sq, int d);
+
+/*
+ * Backward pass by recomputation.  Given the forward's inputs, its bf16
+ * output o and its lse, and the upstream gradient dout:
+ *   D_i = rowsum(dO * O),  P = exp(scale * Q K^T - LSE) on visible entries,
+ *   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+ *   dQ = scale * dS K,  dK = scale * dS^T Q,
+ * with dK/dV of a KV head summed over its query heads.  dq [B,Hq,Sq,d],
+ * dk/dv [B,Hkv,Sk,d] are written (bf16).  The mask arguments, causal flag and
+ * scale must be the ones the forward used.  workspace must hold at least
+ * fa_bwd_workspace_size(B, Hq, Sq, d) bytes; its contents on entry are
+ * ignored and on return are unspecified.
+ * Follows: FlashAttention_01 page, "why the backward can recompute" and the
+ * chain-rule section (dV, dP, dS, dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)).
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+                 int Sk, int d, int causal, float scale, const int32_t* k_start,
+                 const int32_t* k_end, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream);
+
+/* Bytes of device workspace fa_decode needs for a cache of Sk_max positions:
+   per (b, query head, split) partial outputs and logsumexps. */
+size_t fa_decode_workspace_size(int B, int Hq, int Sk_max, int d);
+
+/*
+ * Single-query decode (Sq = 1) over a padded KV cache with split-KV and a
+ * logsumexp merge.  q [B,Hq,1,d]; k_cache/v_cache [B,Hkv,Sk_max,d] of which
+ * the first seqlens_k[b] positions of batch row b are valid; seqlens_k is a
+ * device int32[B] (values clamped to [0, Sk_max]; 0 gives O = 0, LSE = -inf).
+ * o [B,Hq,1,d] is written; lse [B,Hq] is written when not NULL.  The split
+ * plan depends only on (B, Hq, Hkv, Sk_max, d), never on the values in
+ * seqlens_k, so the call never reads device memory on the host.
+ * workspace must hold fa_decode_workspace_size(B, Hq, Sk_max, d) bytes.
+ * Follows: FlashAttention_01 page, "performance validation" (prefill with
+ * Sq = Sk and decode with Sq = 1 are measured separately); the merge applies
+ * the rescale rule of the "Flash Attention" history page 1.2 to whole
+ * per-chunk states.
+ */
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o,
+                    float* lse, const int32_t* seqlens_k, int B, int Hq, int Hkv, int Sk_max,
+                    int d, float scale, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream);
+
+/* Reads the device status words of the current device (this synchronises the
+   device).  Returns FA_OK or FA_ERR_TIMEOUT; *code_out (may be NULL) receives
+   the raw word (low 16 bits: error code, high 16 bits: wait site).  When
+   clear != 0 the words are reset to 0 afterwards. */
+fa_status fa_device_status(unsigned int* code_out, int clear);
+
+/* Static text for a status code. */
+const char* fa_status_string(fa_status s);
+
+/* One-line detail of the last non-OK status returned on the calling thread
+   ("" when none). */
+const char* fa_last_error_detail(void);
+
+/* Library version string. */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

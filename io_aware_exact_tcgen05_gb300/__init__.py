@@ -1,0 +1,178 @@
+"""GB300-native exact tiled attention: thin Python binding over libfa.so.
+
+Every function here only marshals arguments (device pointers, sizes, the
+current CUDA stream) into the C ABI declared in ``include/fa.h``; all of the
+attention arithmetic runs in the library's sm_103a kernels.  PyTorch is used
+only to allocate device memory and to provide streams.  There is no CPU or
+PyTorch fallback: if ``libfa.so`` is missing or fails to load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_WORKSPACE = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+
+EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_decode", "fa_decode_workspace_size",
+            "fa_device_status", "fa_status_string", "fa_last_error_detail", "fa_version")
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: status {status}: {detail}")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libfa.so (build it first with ``io_aware_exact_tcgen05_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfa.so not found at {path}: run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P]
+    lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, Z, P]
+    lib.fa_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P, Z, P]
+    lib.fa_bwd_workspace_size.argtypes = [I, I, I, I]
+    lib.fa_bwd_workspace_size.restype = Z
+    lib.fa_decode_workspace_size.argtypes = [I, I, I, I]
+    lib.fa_decode_workspace_size.restype = Z
+    lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
+    for f in (lib.fa_fwd, lib.fa_bwd, lib.fa_decode, lib.fa_device_status):
+        f.restype = I
+    lib.fa_status_string.argtypes = [I]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_error_detail.restype = ctypes.c_char_p
+    lib.fa_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != FA_OK:
+        detail = _lib.fa_last_error_detail().decode()
+        raise FAError(status, where, detail or _lib.fa_status_string(status).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def fa_fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, o=None, lse=None,
+           stream=None):
+    """O, LSE = attention(q, k, v) via the library's fa_fwd (see include/fa.h).
+    q [B,Hq,Sq,d], k/v [B,Hkv,Sk,d] bf16 CUDA tensors; k_start/k_end optional
+    int32 [B] CUDA tensors.  Returns (o, lse)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Hq, Sq, d = q.shape
+    _, Hkv, Sk, _ = k.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q.device)
+    for t, n in ((k_start, "k_start"), (k_end, "k_end")):
+        if t is not None:
+            _need(t, n, torch.int32, 1)
+    st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
+                    int(bool(causal)), float(scale), _ptr(k_start), _ptr(k_end), _stream(stream))
+    _check(st, "fa_fwd")
+    return o, lse
+
+
+def fa_bwd_workspace_size(B, Hq, Sq, d) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, Hq, Sq, d))
+
+
+def fa_bwd(q, k, v, o, dout, lse, causal: bool, scale: float, k_start=None, k_end=None,
+           dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV by recomputation via the library's fa_bwd.  Returns (dq, dk, dv)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    B, Hq, Sq, d = q.shape
+    _, Hkv, Sk, _ = k.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = fa_bwd_workspace_size(B, Hq, Sq, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                    _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d, int(bool(causal)), float(scale),
+                    _ptr(k_start), _ptr(k_end), _ptr(workspace), workspace.numel(),
+                    _stream(stream))
+    _check(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_decode_workspace_size(B, Hq, Sk_max, d) -> int:
+    return int(load_library().fa_decode_workspace_size(B, Hq, Sk_max, d))
+
+
+def fa_decode(q, k_cache, v_cache, seqlens_k, scale: float, o=None, lse=None, workspace=None,
+              stream=None):
+    """Single-query decode over a padded cache via the library's fa_decode.
+    q [B,Hq,1,d], k_cache/v_cache [B,Hkv,Sk_max,d], seqlens_k int32 [B] (CUDA).
+    Returns (o [B,Hq,1,d], lse [B,Hq])."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(seqlens_k, "seqlens_k", torch.int32, 1)
+    B, Hq, _, d = q.shape
+    _, Hkv, Sk_max, _ = k_cache.shape
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device) if lse is None else lse
+    nbytes = fa_decode_workspace_size(B, Hq, Sk_max, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    st = lib.fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
+                       _ptr(seqlens_k), B, Hq, Hkv, Sk_max, d, float(scale), _ptr(workspace),
+                       workspace.numel(), _stream(stream))
+    _check(st, "fa_decode")
+    return o, lse
+
+
+def fa_device_status(clear: bool = True):
+    """(status, raw word) of the device status words; synchronises the device."""
+    lib = load_library()
+    w = ctypes.c_uint(0)
+    st = lib.fa_device_status(ctypes.byref(w), int(bool(clear)))
+    return st, w.value
+
+
+def version() -> str:
+    return load_library().fa_version().decode()

@@ -1,0 +1,323 @@
+// fa_api.cu -- the extern "C" boundary of libfa.so (declared in include/fa.h):
+// argument validation, TMA tensor-map encoding, workspace carving and kernel
+// launch.  No device memory is allocated here; no device memory is read on the
+// host (the calls stay asynchronous and capturable).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+thread_local char g_detail[256] = "";
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+fa_status ok() {
+  g_detail[0] = '\0';
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device check: the kernels are built for sm_103a only.
+fa_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  static int cached_major[64], cached_minor[64];
+  static bool cached[64];
+  if (dev < 0 || dev >= 64) return fail(FA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  if (!cached[dev]) {
+    int ma = 0, mi = 0;
+    cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev);
+    cached_major[dev] = ma;
+    cached_minor[dev] = mi;
+    cached[dev] = true;
+  }
+  if (cached_major[dev] != 10 || cached_minor[dev] != 3)
+    return fail(FA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                dev, cached_major[dev], cached_minor[dev]);
+  return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [heads, rows, d] bf16 tensor, 128-row x 64-column boxes, 128-byte swizzle;
+// rows past the end of a head read as zero.
+fa_status make_map(CUtensorMap* map, const void* base, long heads, long rows, int d) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(fa::kTileM), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return FA_OK;
+}
+
+fa_status check_sizes(int B, int Hq, int Hkv, int Sq, int Sk, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1)
+    return fail(FA_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d Hq=%d Hkv=%d Sq=%d Sk=%d)", B, Hq,
+                Hkv, Sq, Sk);
+  if (Hq % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "Hq (%d) %% Hkv (%d) != 0", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension %d (want 64 or 128)", d);
+  // TMA coordinates are int32 and the head count is a tensor-map extent
+  const long long rows_q = 1LL * B * Hq * Sq, rows_k = 1LL * B * Hkv * Sk;
+  if (rows_q >= (1LL << 31) || rows_k >= (1LL << 31))
+    return fail(FA_ERR_INVALID_ARG, "tensor too large for 32-bit row indices");
+  return FA_OK;
+}
+
+fa_status check_ptr(const void* p, const char* name, bool nullable = false) {
+  if (!p) return nullable ? FA_OK : fail(FA_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(FA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return FA_OK;
+}
+
+fa_status check_i32(const void* p, const char* name) {
+  if (p && (reinterpret_cast<uintptr_t>(p) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "%s is not 4-byte aligned", name);
+  return FA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+#define FA_TRY(expr)                 \
+  do {                               \
+    fa_status _s = (expr);           \
+    if (_s != FA_OK) return _s;      \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                 const int32_t* k_start, const int32_t* k_end, cudaStream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, Sq, Sk, d));
+  FA_TRY(check_ptr(q, "q"));
+  FA_TRY(check_ptr(k, "k"));
+  FA_TRY(check_ptr(v, "v"));
+  FA_TRY(check_ptr(o, "o"));
+  FA_TRY(check_ptr(lse, "lse", true));
+  FA_TRY(check_i32(k_start, "k_start"));
+  FA_TRY(check_i32(k_end, "k_end"));
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale is not finite");
+  FA_TRY(check_device());
+
+  CUtensorMap tq, tk, tv;
+  FA_TRY(make_map(&tq, q, 1L * B * Hq, Sq, d));
+  FA_TRY(make_map(&tk, k, 1L * B * Hkv, Sk, d));
+  FA_TRY(make_map(&tv, v, 1L * B * Hkv, Sk, d));
+
+  fa::FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.k_start = k_start;
+  p.k_end = k_end;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.group = Hq / Hkv;
+  p.pack_heads = (p.group % 2 == 0) ? 1 : 0;
+  const int n_rb = (Sq + fa::kTileM - 1) / fa::kTileM;
+  if (p.pack_heads) {
+    p.n_rbu = n_rb;
+    p.units_per_rbu = B * (Hq / 2);
+  } else {
+    p.n_rbu = (n_rb + 1) / 2;
+    p.units_per_rbu = B * Hq;
+  }
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.rescale_log2 = 8.0f;
+  if (1LL * p.n_rbu * p.units_per_rbu >= (1LL << 31))
+    return fail(FA_ERR_INVALID_ARG, "grid too large");
+  cudaError_t e = fa::launch_fwd(d, tq, tk, tv, p, stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "fa_fwd launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+size_t fa_decode_workspace_size(int B, int Hq, int Sk_max, int d) {
+  if (B < 1 || Hq < 1 || Sk_max < 1 || d < 1) return 0;
+  int chunk = 0, n_split = 0;
+  fa::decode_plan(B, Hq, 1, Sk_max, &chunk, &n_split);
+  const size_t rows = static_cast<size_t>(B) * Hq * n_split;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    const int32_t* seqlens_k, int B, int Hq, int Hkv, int Sk_max, int d,
+                    float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, 1, Sk_max, d));
+  FA_TRY(check_ptr(q, "q"));
+  FA_TRY(check_ptr(k_cache, "k_cache"));
+  FA_TRY(check_ptr(v_cache, "v_cache"));
+  FA_TRY(check_ptr(o, "o"));
+  FA_TRY(check_ptr(lse, "lse", true));
+  if (!seqlens_k) return fail(FA_ERR_INVALID_ARG, "seqlens_k is NULL");
+  FA_TRY(check_i32(seqlens_k, "seqlens_k"));
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale is not finite");
+  const size_t need = fa_decode_workspace_size(B, Hq, Sk_max, d);
+  if (!workspace || workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "decode workspace needs %zu bytes, got %zu", need,
+                workspace ? workspace_bytes : size_t(0));
+  FA_TRY(check_ptr(workspace, "workspace"));
+  FA_TRY(check_device());
+
+  fa::DecodeParams p{};
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.o = o;
+  p.lse = lse;
+  p.seqlens = seqlens_k;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sk_max = Sk_max;
+  p.group = Hq / Hkv;
+  fa::decode_plan(B, Hq, Hkv, Sk_max, &p.chunk, &p.n_split);
+  const size_t rows = static_cast<size_t>(B) * Hq * p.n_split;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        align256(rows * d * sizeof(float)));
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  if (p.n_split > 65535 * 64 || 1LL * B > 65535)
+    return fail(FA_ERR_INVALID_ARG, "decode grid too large");
+  cudaError_t e = fa::launch_decode(d, p, stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "fa_decode launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+size_t fa_bwd_workspace_size(int B, int Hq, int Sq, int d) {
+  if (B < 1 || Hq < 1 || Sq < 1 || d < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * Sq;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+                 int Sk, int d, int causal, float scale, const int32_t* k_start,
+                 const int32_t* k_end, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, Sq, Sk, d));
+  FA_TRY(check_ptr(q, "q"));
+  FA_TRY(check_ptr(k, "k"));
+  FA_TRY(check_ptr(v, "v"));
+  FA_TRY(check_ptr(o, "o"));
+  FA_TRY(check_ptr(dout, "dout"));
+  FA_TRY(check_ptr(lse, "lse"));
+  FA_TRY(check_ptr(dq, "dq"));
+  FA_TRY(check_ptr(dk, "dk"));
+  FA_TRY(check_ptr(dv, "dv"));
+  FA_TRY(check_i32(k_start, "k_start"));
+  FA_TRY(check_i32(k_end, "k_end"));
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale is not finite");
+  const size_t need = fa_bwd_workspace_size(B, Hq, Sq, d);
+  if (!workspace || workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "backward workspace needs %zu bytes, got %zu", need,
+                workspace ? workspace_bytes : size_t(0));
+  FA_TRY(check_ptr(workspace, "workspace"));
+  FA_TRY(check_device());
+
+  CUtensorMap tq, tk, tv, tdo;
+  FA_TRY(make_map(&tq, q, 1L * B * Hq, Sq, d));
+  FA_TRY(make_map(&tk, k, 1L * B * Hkv, Sk, d));
+  FA_TRY(make_map(&tv, v, 1L * B * Hkv, Sk, d));
+  FA_TRY(make_map(&tdo, dout, 1L * B * Hq, Sq, d));
+
+  fa::BwdParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  const size_t rows = static_cast<size_t>(B) * Hq * Sq;
+  p.dq_acc = static_cast<float*>(workspace);
+  p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                     align256(rows * d * sizeof(float)));
+  p.k_start = k_start;
+  p.k_end = k_end;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.group = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  cudaError_t e = fa::launch_bwd(d, tq, tk, tv, tdo, p, stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "fa_bwd launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+fa_status fa_device_status(unsigned int* code_out, int clear) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+  const unsigned int w = fa::read_fwd_status(clear != 0) | fa::read_decode_status(clear != 0) |
+                         fa::read_bwd_status(clear != 0);
+  if (code_out) *code_out = w;
+  if (w != 0) return fail(FA_ERR_TIMEOUT, "device status word 0x%08x", w);
+  return ok();
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* fa_last_error_detail(void) { return g_detail; }
+
+const char* fa_version(void) { return "io_aware_exact_tcgen05_gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

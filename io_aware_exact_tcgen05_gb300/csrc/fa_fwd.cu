@@ -1,0 +1,414 @@
+// fa_fwd.cu -- forward attention kernel for sm_103a (tcgen05 + TMEM + TMA).
+//
+// One CTA owns two 128-row query tiles ("slots") that share every key/value
+// tile it streams: either two query heads of one KV group at the same rows
+// (grouped heads: K/V tiles are fetched once per KV head for both), or two
+// consecutive row blocks of one head.  Per key/value tile j:
+//
+//   S_t = Q_t K_j^T          tcgen05.mma, A and B from shared memory, fp32 in TMEM
+//   softmax warps of slot t  tcgen05.ld S_t (one TMEM lane = one query row = one
+//                            thread), mask, row max, conditional rescale of O_t,
+//                            p = 2^(s*c - m*c), row sum, P_t -> bf16 into the
+//                            TMEM columns of S_t
+//   O_t += P_t V_j           tcgen05.mma, A (P) from TMEM, B (V) from shared memory
+//
+// The two slots ping-pong: while the softmax warps of one slot work, the
+// tensor core runs the other slot's MMAs.  The S x S matrix never leaves
+// TMEM/registers; O is divided by l once at the end and the per-row
+// logsumexp is written beside it.
+//
+// Method: "Flash Attention" history page 1.2 (running max, denominator and
+// rescaled output), 1.3 (tiles discarded on chip), 2.1 (query-sequence
+// parallelism, fully masked causal tiles skipped), 2.3 (asynchronous MMA and
+// skipping the rescale while the running max does not grow); FlashAttention_01
+// page, online-softmax derivation (m, l, u; mask before the max; empty rows).
+//
+// Warp roles (320 threads): warps 0-3 softmax of slot 0, warps 4-7 softmax of
+// slot 1 (a warp may only touch TMEM lanes 32*(warp%4) .. +31, which are the
+// rows it owns), warp 8 TMA producer, warp 9 MMA issuer and TMEM owner.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+
+// wait-site ids reported in the status word
+enum : unsigned int {
+  kSiteQ = 1, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSitePFull, kSiteSFull,
+  kSiteOFull, kSiteDrain
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr int NB = D / 64;               // 64-wide (128-byte) column blocks per row
+  static constexpr int NS = (D == 128) ? 2 : 3;   // K and V pipeline depth
+  static constexpr int kBox = kTileM * 64;        // elements per 128-row x 64-col box
+  __nv_bfloat16 q[2][NB][kBox];
+  __nv_bfloat16 k[NS][NB][kBox];
+  __nv_bfloat16 v[NS][NB][kBox];
+  uint64_t bar_q;
+  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t drain;  // MMA teardown after an abort
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+constexpr size_t fwd_smem_bytes() {
+  return sizeof(FwdSmem<D>) + 1024;  // + alignment slack
+}
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  using Smem = FwdSmem<D>;
+  constexpr int NB = Smem::NB;
+  constexpr int NS = Smem::NS;
+  constexpr uint32_t kBoxBytes = Smem::kBox * 2;
+  extern __shared__ unsigned char smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: heavy (late) row blocks are launched first -------------
+  const int L = blockIdx.x;
+  const int rbu = p.n_rbu - 1 - L / p.units_per_rbu;
+  const int u = L % p.units_per_rbu;
+  int b, h0, h1, r0, r1;
+  if (p.pack_heads) {
+    const int hpairs = p.Hq >> 1;
+    b = u / hpairs;
+    h0 = 2 * (u % hpairs);
+    h1 = h0 + 1;
+    r0 = r1 = rbu * kTileM;
+  } else {
+    b = u / p.Hq;
+    h0 = h1 = u % p.Hq;
+    r0 = rbu * 2 * kTileM;
+    r1 = r0 + kTileM;
+  }
+  const bool active1 = r1 < p.Sq;
+  const int hk = h0 / p.group;
+
+  int klo = p.k_start ? p.k_start[b] : 0;
+  int kend = p.k_end ? p.k_end[b] : p.Sk;
+  klo = max(0, min(klo, p.Sk));
+  kend = max(0, min(kend, p.Sk));
+  const int off = p.Sk - p.Sq;  // bottom-right causal alignment
+  int khi = kend;
+  if (p.causal) {
+    const int last_row = min((active1 ? r1 : r0) + kTileM - 1, p.Sq - 1);
+    khi = min(khi, last_row + off + 1);
+  }
+  int j0 = 0, n_tiles = 0;
+  if (khi > klo) {
+    j0 = klo / kTileN;
+    n_tiles = (khi + kTileN - 1) / kTileN - j0;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&s.bar_q, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_empty[i], 1);
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.v_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s.s_full[t], 1);
+      mbar_init(&s.p_full[t], 4 * 32);
+      mbar_init(&s.o_full[t], 1);
+    }
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 8) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      const uint64_t keep = policy_evict_last();
+      mbar_arrive_expect_tx(&s.bar_q, (active1 ? 2 : 1) * NB * kBoxBytes);
+      for (int cb = 0; cb < NB; ++cb) {
+        tma_load_3d(s.q[0][cb], &tq, &s.bar_q, cb * 64, r0, b * p.Hq + h0);
+        if (active1) tma_load_3d(s.q[1][cb], &tq, &s.bar_q, cb * 64, r1, b * p.Hq + h1);
+      }
+      const int zkv = b * p.Hkv + hk;
+      int k_issued = 0, v_issued = 0;  // tiles whose loads were issued
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % NS;
+        const int use = j / NS;
+        const int c0 = (j0 + j) * kTileN;
+        if (use > 0 && !mbar_wait(&s.k_empty[st], (use - 1) & 1, abort_flag, kSiteKEmpty)) break;
+        mbar_arrive_expect_tx(&s.k_full[st], NB * kBoxBytes);
+        for (int cb = 0; cb < NB; ++cb)
+          tma_load_3d_hint(s.k[st][cb], &tk, &s.k_full[st], cb * 64, c0, zkv, keep);
+        k_issued = j + 1;
+        if (use > 0 && !mbar_wait(&s.v_empty[st], (use - 1) & 1, abort_flag, kSiteVEmpty)) break;
+        mbar_arrive_expect_tx(&s.v_full[st], NB * kBoxBytes);
+        for (int cb = 0; cb < NB; ++cb)
+          tma_load_3d_hint(s.v[st][cb], &tv, &s.v_full[st], cb * 64, c0, zkv, keep);
+        v_issued = j + 1;
+      }
+      if (*abort_flag) {
+        // let every issued copy land before shared memory is released
+        mbar_drain(&s.bar_q, 0, kSiteDrain);
+        for (int j = max(0, k_issued - NS); j < k_issued; ++j)
+          mbar_drain(&s.k_full[j % NS], (j / NS) & 1, kSiteDrain);
+        for (int j = max(0, v_issued - NS); j < v_issued; ++j)
+          mbar_drain(&s.v_full[j % NS], (j / NS) & 1, kSiteDrain);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, false, true);
+      const int nslots = active1 ? 2 : 1;
+      bool ok = mbar_wait(&s.bar_q, 0, abort_flag, kSiteQ);
+      tc_fence_after();
+      for (int j = 0; ok && j <= n_tiles; ++j) {
+        if (j < n_tiles) {
+          if (!mbar_wait(&s.k_full[j % NS], (j / NS) & 1, abort_flag, kSiteKFull)) break;
+          tc_fence_after();
+        }
+        for (int t = 0; t < nslots; ++t) {
+          const uint32_t t_s = tmem + t * kTileN;
+          if (j > 0) {
+            // O_t += P_t(j-1) V_{j-1}; P_t lives in the first 64 columns of S_t
+            if (!mbar_wait(&s.p_full[t], (j - 1) & 1, abort_flag, kSitePFull)) { ok = false; break; }
+            const int vs = (j - 1) % NS;
+            if (t == 0 && !mbar_wait(&s.v_full[vs], ((j - 1) / NS) & 1, abort_flag, kSiteVFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t t_o = tmem + 2 * kTileN + t * D;
+            const uint32_t v0 = smem_u32(s.v[vs][0]);
+            const uint32_t lbo = (NB > 1) ? (smem_u32(s.v[vs][NB - 1]) - v0) : 16u;
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 16; ++kk) {
+              const uint64_t bdesc = smem_desc_sw128(v0 + kk * 16 * 128, lbo, 1024);
+              mma_ts(t_o, t_s + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          if (j < n_tiles) {
+            // S_t = Q_t K_j^T
+            const int ks = j % NS;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t adesc =
+                  smem_desc_sw128(smem_u32(s.q[t][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+              const uint64_t bdesc =
+                  smem_desc_sw128(smem_u32(s.k[ks][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+              mma_ss(t_s, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s.s_full[t]);
+          } else {
+            mma_commit(&s.o_full[t]);
+          }
+        }
+        if (!ok) break;
+        if (j > 0) mma_commit(&s.v_empty[(j - 1) % NS]);
+        if (j < n_tiles) mma_commit(&s.k_empty[j % NS]);
+      }
+      if (*abort_flag) {
+        // every MMA issued so far must finish before TMEM is released
+        mma_commit(&s.drain);
+        mbar_drain(&s.drain, 0, kSiteDrain);
+      }
+    }
+  } else {
+    // ---------------------------------------------------- softmax warps --
+    const int t = warp >> 2;
+    const int row_in_tile = (warp & 3) * 32 + lane;
+    const int i = (t == 0 ? r0 : r1) + row_in_tile;
+    const int h = (t == 0) ? h0 : h1;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + t * kTileN + lane_off;
+    const uint32_t t_o = tmem + 2 * kTileN + t * D + lane_off;
+    const float c = p.scale_log2;
+    // keys visible to this row: [klo, khi_row)
+    int khi_row = kend;
+    if (p.causal) khi_row = min(khi_row, i + off + 1);
+    float m = neg_inf();  // running max of raw scores (unscaled)
+    float l = 0.f;        // running denominator, relative to 2^(m*c)
+    float lr = 0.f;       // same, over the bf16-rounded weights
+    bool ok = (t == 0) || active1;
+    if (ok && n_tiles > 0) {
+      for (int j = 0; j < n_tiles; ++j) {
+        if (!mbar_wait(&s.s_full[t], j & 1, abort_flag, kSiteSFull)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[kTileN];
+#pragma unroll
+        for (int cc = 0; cc < kTileN / 32; ++cc)
+          tmem_ld32(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+        tmem_wait_ld();
+        const int c0 = (j0 + j) * kTileN;
+        const bool need_mask = (c0 < klo) || (c0 + kTileN > khi_row);
+        if (__any_sync(0xffffffffu, need_mask)) {
+#pragma unroll
+          for (int jj = 0; jj < kTileN; ++jj) {
+            const int key = c0 + jj;
+            if (key < klo || key >= khi_row) sr[jj] = 0xff800000u;
+          }
+        }
+        // row max with 8 independent chains (short dependency chains)
+        float mx8[8];
+#pragma unroll
+        for (int q2 = 0; q2 < 8; ++q2) mx8[q2] = __uint_as_float(sr[q2]);
+#pragma unroll
+        for (int jj = 8; jj < kTileN; ++jj) mx8[jj & 7] = fmaxf(mx8[jj & 7], __uint_as_float(sr[jj]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float m_new = fmaxf(m, mx);
+        // (m_new - m) is NaN only when both are -inf: no rescale then.
+        const bool grow = (m_new - m) * c > p.rescale_log2;
+        const float alpha = grow ? ex2_approx((m - m_new) * c) : 1.f;  // 0 when m = -inf
+        if (grow) {
+          l *= alpha;
+          lr *= alpha;
+          m = m_new;
+        }
+        const float mc = (m == neg_inf()) ? 0.f : m * c;
+        // l sums the fp32 weights (it gives the LSE); lr sums the bf16-rounded
+        // weights the PV MMA actually multiplies, so O = u / lr is an exactly
+        // normalised combination of the V rows
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        float sumr4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[kTileN / 2];
+#pragma unroll
+        for (int jj = 0; jj < kTileN / 2; ++jj) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * jj]), c, -mc));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * jj + 1]), c, -mc));
+          sum4[jj & 3] += p0 + p1;
+          pk[jj] = pack_bf16x2(p0, p1);
+          sumr4[jj & 3] += __uint_as_float(pk[jj] << 16) + __uint_as_float(pk[jj] & 0xffff0000u);
+        }
+        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        lr += (sumr4[0] + sumr4[1]) + (sumr4[2] + sumr4[3]);
+        tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // O_t is quiescent here: PV_t(j-1) completed before S_t(j) was
+          // signalled, and PV_t(j) is issued only after p_full below.
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t orr[32];
+            tmem_ld32(t_o + cc * 32, orr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q2 = 0; q2 < 32; ++q2)
+              orr[q2] = __float_as_uint(__uint_as_float(orr[q2]) * alpha);
+            tmem_st32(t_o + cc * 32, orr);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&s.p_full[t]);
+      }
+      if (ok) ok = mbar_wait(&s.o_full[t], 0, abort_flag, kSiteOFull);
+      tc_fence_after();
+    }
+    // ---- epilogue: O = u / l, LSE = m*scale + ln l ---------------------
+    if (((t == 0) || active1) && !*abort_flag) {
+      const bool live = l > 0.f;
+      const float inv = live ? 1.f / lr : 0.f;
+      const bool in_range = i < p.Sq;
+      const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Sq + i;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t orr[32];
+        if (n_tiles > 0) {
+          tmem_ld32(t_o + cc * 32, orr);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int q2 = 0; q2 < 32; ++q2) orr[q2] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int q2 = 0; q2 < 16; ++q2)
+          pk[q2] = pack_bf16x2(__uint_as_float(orr[2 * q2]) * inv,
+                               __uint_as_float(orr[2 * q2 + 1]) * inv);
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2)
+            dst[q2] = make_uint4(pk[4 * q2], pk[4 * q2 + 1], pk[4 * q2 + 2], pk[4 * q2 + 3]);
+        }
+      }
+      if (in_range && p.lse) p.lse[row] = live ? fmaf(m, p.scale, logf(l)) : neg_inf();
+    }
+  }
+
+  // ---- teardown ----------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, cudaStream_t stream) {
+  constexpr size_t smem = fwd_smem_bytes<D>();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned int grid = static_cast<unsigned int>(p.n_rbu) * p.units_per_rbu;
+  fa_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, cudaStream_t stream) {
+  if (d == 128) return launch_fwd_d<128>(tq, tk, tv, p, stream);
+  return launch_fwd_d<64>(tq, tk, tv, p, stream);
+}
+
+unsigned int read_fwd_status(bool clear) {
+  unsigned int v = 0;
+  cudaMemcpyFromSymbol(&v, g_status, sizeof v);
+  if (clear) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_status, &z, sizeof z);
+  }
+  return v;
+}
+
+}  // namespace fa

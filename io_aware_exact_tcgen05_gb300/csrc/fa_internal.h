@@ -1,0 +1,83 @@
+// fa_internal.h -- parameter blocks and launch entry points shared between
+// the C-ABI layer (fa_api.cu) and the kernel translation units.  Host-side
+// only declarations plus plain structs; no device code.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace fa {
+
+// Rows of one query tile and keys of one key/value tile in the tensor-core
+// kernels (one tcgen05.mma M=128 accumulator; 128 TMEM lanes).
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+
+struct FwdParams {
+  void* o;             // bf16 [B,Hq,Sq,d]
+  float* lse;          // fp32 [B,Hq,Sq] or nullptr
+  const int32_t* k_start;
+  const int32_t* k_end;
+  int B, Hq, Hkv, Sq, Sk;
+  int group;           // Hq / Hkv
+  int pack_heads;      // 1: a CTA's two query tiles are two heads of one KV group
+  int n_rbu;           // row-block units per (b, head unit)
+  int units_per_rbu;   // (b, head unit) pairs
+  int causal;
+  float scale;         // natural-log softmax scale
+  float scale_log2;    // scale * log2(e)
+  float rescale_log2;  // skip the O rescale unless the max grows by more than this (log2 units)
+};
+
+// Launch the forward kernel for head dimension d (64 or 128).
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream);
+unsigned int read_fwd_status(bool clear);
+
+struct DecodeParams {
+  const void* q;        // bf16 [B,Hq,1,d]
+  const void* k;        // bf16 [B,Hkv,Sk_max,d]
+  const void* v;
+  void* o;              // bf16 [B,Hq,1,d]
+  float* lse;           // fp32 [B,Hq] or nullptr
+  const int32_t* seqlens;
+  float* part_o;        // fp32 [B,Hq,n_split,d]
+  float* part_lse;      // fp32 [B,Hq,n_split]
+  int B, Hq, Hkv, Sk_max, group;
+  int chunk;            // keys per split
+  int n_split;
+  float scale_log2;
+};
+
+cudaError_t launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
+unsigned int read_decode_status(bool clear);
+void decode_plan(int B, int Hq, int Hkv, int Sk_max, int* chunk, int* n_split);
+
+struct BwdParams {
+  const void* q;        // bf16 [B,Hq,Sq,d]
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;     // fp32 [B,Hq,Sq]
+  void* dq;             // bf16 out
+  void* dk;
+  void* dv;
+  float* dq_acc;        // fp32 [B,Hq,Sq,d] workspace
+  float* delta;         // fp32 [B,Hq,Sq] workspace: D_i
+  const int32_t* k_start;
+  const int32_t* k_end;
+  int B, Hq, Hkv, Sq, Sk, group;
+  int causal;
+  float scale;
+  float scale_log2;
+};
+
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                       cudaStream_t stream);
+unsigned int read_bwd_status(bool clear);
+
+}  // namespace fa

@@ -8,11 +8,11 @@ draws, in this order, Q, K, V and then dO (when the workload has a backward),
 each as i.i.d. N(0, 1) in fp32, in the [B, H, S, d] layout, and each is then
 rounded to bf16 (round to nearest even).  Workload-specific extras:
 
-* ``prefill_large_logits``: Q is multiplied by 8 before rounding, so raw
+* ``prefill_8k_masked``: Q is multiplied by 8 before rounding, so raw
   logits reach about +-100 and a naive exp would overflow; batch row 0 gets
   the key interval [64, Sk), i.e. keys 0..63 are padding, which under the
   causal rule leaves query rows 0..63 of that batch row with no visible key.
-* ``decode``: per-sequence key lengths are drawn first, uniform integers in
+* ``decode_ragged``: per-sequence key lengths are drawn first, uniform integers in
   [1024, 32768], from the same seeded generator; the KV cache is padded to
   32768 positions and the padding is left at zero.
 """
@@ -131,3 +131,16 @@ def worked_example_bf16():
     v = torch.zeros(1, 1, 3, d)
     v[0, 0, :, 0] = torch.tensor([1.0, 3.0, 7.0])
     return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def random_qkv(B, Hq, Hkv, Sq, Sk, d, seed=0, q_mult=1.0, with_dout=False):
+    """Seeded bf16 Q, K, V (and dO) of arbitrary shape, same recipe as ``make``."""
+    gen = torch.Generator().manual_seed(seed)
+    out = {
+        "q": _randn(gen, (B, Hq, Sq, d), q_mult),
+        "k": _randn(gen, (B, Hkv, Sk, d)),
+        "v": _randn(gen, (B, Hkv, Sk, d)),
+    }
+    if with_dout:
+        out["dout"] = _randn(gen, (B, Hq, Sq, d))
+    return out

