@@ -1,14 +1,511 @@
-// fa_bwd.cu -- backward attention kernels (placeholder until the tcgen05
-// backward lands; returns cudaErrorNotYetImplemented).
+// fa_bwd.cu -- backward attention by recomputation for sm_103a.
+//
+//   1. fa_bwd_pre:   D_i = rowsum(dO_i * O_i) (fp32) and dQacc = 0
+//   2. fa_bwd_main:  one CTA per (128-key tile, KV head, batch row).  K and V
+//                    stay in shared memory; the CTA walks every query head of
+//                    the group and every 128-row query tile that can see its
+//                    keys.  Per query tile (all five contractions on tcgen05):
+//        S^T  = K Q^T            (keys x queries, fp32 in TMEM)
+//        dP^T = V dO^T           (keys x queries, fp32 in TMEM)
+//        P^T  = exp(scale*S^T - LSE) on visible entries, 0 elsewhere
+//               -> bf16 back into the S^T columns           [compute warps]
+//        dV  += P^T dO           (A = P^T from TMEM)
+//        dS^T = P^T * (dP^T - D) -> bf16 into the dP^T columns and into
+//               shared memory                               [compute warps]
+//        dK  += dS^T Q           (A = dS^T from TMEM)
+//        dQ   = dS K             (A = dS from shared memory, written into the
+//                                 dP^T columns, which are free by then)
+//        dQacc += dQ             fp32 vector atomics        [drain warps]
+//      At the end dK (times scale) and dV leave TMEM as bf16.  With grouped
+//      heads dK/dV already hold the sum over the group's query heads.
+//   3. fa_bwd_convert: dQ = bf16(scale * dQacc)
+//
+// Method: FlashAttention_01 page, "why the backward can recompute" (rebuild P
+// from the saved per-row logsumexp; dV and dP first, then dS from the softmax
+// Jacobian, then dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)) and the chain-rule
+// section (masked probabilities and their score gradients are 0); the same
+// mask, statistics and scale as the forward.
+//
+// Warp roles (320 threads): warps 0-3 compute (one key row = one TMEM lane per
+// thread), warps 4-7 drain dQ (one query row per thread), warp 8 TMA producer,
+// warp 9 MMA issuer and TMEM owner.
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
 namespace fa {
-cudaError_t launch_bwd(int, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                       const CUtensorMap&, const BwdParams&, cudaStream_t) {
-  return cudaErrorNotYetImplemented;
+namespace {
+
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kQStages = 2;
+
+enum : unsigned int {
+  kSiteKV = 1, kSiteQFull, kSiteQEmpty, kSiteS, kSiteP, kSiteDP, kSiteDS, kSiteDQFull,
+  kSiteDQEmpty, kSiteDKV, kSiteDrain, kSiteAlign, kSiteStat
+};
+
+template <int D>
+struct BwdSmem {
+  static constexpr int NB = D / 64;
+  static constexpr int kBox = kTileM * 64;
+  __nv_bfloat16 k[NB][kBox];
+  __nv_bfloat16 v[NB][kBox];
+  __nv_bfloat16 q[kQStages][NB][kBox];
+  __nv_bfloat16 dout[kQStages][NB][kBox];
+  __nv_bfloat16 ds[2][kBox];        // dS^T rows = keys, two 64-query blocks, 128B swizzle
+  float lse2[2][kTileM];            // LSE * log2(e), +inf for rows without keys
+  float delta[2][kTileM];           // D_i; both double-buffered by tile parity
+  uint64_t stat_ready[2];
+  uint64_t kv_full;
+  uint64_t q_full[kQStages], q_empty[kQStages];
+  uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_empty, dkv_full, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+__device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
 }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// ------------------------------------------------------------ preprocess --
+// D/8 lanes per row (8 bf16 each): D_i = sum_c dO_ic O_ic; the row of dQacc is zeroed.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre(const BwdParams p, long long rows) {
+  constexpr int LPR = D / 8;
+  const long long row = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / LPR;
+  const int x = threadIdx.x % LPR;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 o = *reinterpret_cast<const uint4*>(
+        reinterpret_cast<const __nv_bfloat16*>(p.o) + row * D + x * 8);
+    const uint4 g = *reinterpret_cast<const uint4*>(
+        reinterpret_cast<const __nv_bfloat16*>(p.dout) + row * D + x * 8);
+    const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(gw[e] << 16), acc);
+      acc = fmaf(__uint_as_float(ow[e] & 0xffff0000u), __uint_as_float(gw[e] & 0xffff0000u), acc);
+    }
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D + x * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int o = LPR / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (row < rows && x == 0) p.delta[row] = acc;
+}
+
+// --------------------------------------------------------------- convert --
+__global__ void __launch_bounds__(256) fa_bwd_convert(const BwdParams p, long long n4) {
+  const long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= n4) return;
+  const float4 a = reinterpret_cast<const float4*>(p.dq_acc)[i];
+  uint2 out;
+  out.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+  out.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
+  reinterpret_cast<uint2*>(p.dq)[i] = out;
+}
+
+// ------------------------------------------------------------------ main --
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_main(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                const BwdParams p) {
+  using Smem = BwdSmem<D>;
+  constexpr int NB = Smem::NB;
+  constexpr uint32_t kBoxBytes = Smem::kBox * 2;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if ((smem_u32(smem_raw) & 1023u) != 0) {  // 128B-swizzle atoms need 1024B alignment
+    if (threadIdx.x == 0) raise_status(2u, kSiteAlign);
+    return;
+  }
+
+  // ---- work unit: key tile (heavy first under the causal rule), KV head, batch
+  const int bh = blockIdx.x % (p.B * p.Hkv);
+  const int kt = blockIdx.x / (p.B * p.Hkv);
+  const int b = bh / p.Hkv;
+  const int hk = bh % p.Hkv;
+  const int c0 = kt * kTileN;
+  int klo = p.k_start ? p.k_start[b] : 0;
+  int kend = p.k_end ? p.k_end[b] : p.Sk;
+  klo = max(0, min(klo, p.Sk));
+  kend = max(0, min(kend, p.Sk));
+  const int off = p.Sk - p.Sq;
+  const int n_qt_all = (p.Sq + kTileM - 1) / kTileM;
+  int qt_lo = 0;
+  if (p.causal) qt_lo = max(0, c0 - off) / kTileM;  // first query row that sees key c0
+  const bool keys_live = (c0 < kend) && (c0 + kTileN > klo) && (!p.causal || c0 - off < p.Sq);
+  const int n_qt = keys_live ? max(0, n_qt_all - qt_lo) : 0;
+  const int n_it = n_qt * p.group;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&s.kv_full, 1);
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&s.q_full[i], 1);
+      mbar_init(&s.q_empty[i], 1);
+    }
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.p_full, 128);
+    mbar_init(&s.dp_full, 1);
+    mbar_init(&s.ds_full, 128);
+    mbar_init(&s.dq_full, 1);
+    mbar_init(&s.dq_empty, 128);
+    mbar_init(&s.dkv_full, 1);
+    mbar_init(&s.drain, 1);
+    mbar_init(&s.stat_ready[0], 128);
+    mbar_init(&s.stat_ready[1], 128);
+    s.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  const uint32_t t_S = tmem;              // S^T, then P^T (bf16, first 64 columns)
+  const uint32_t t_dP = tmem + kTileN;    // dP^T, then dS^T (bf16), then dQ
+  const uint32_t t_dV = tmem + 2 * kTileN;
+  const uint32_t t_dK = tmem + 2 * kTileN + D;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 8) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0 && n_it > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tdo);
+      const int zkv = b * p.Hkv + hk;
+      mbar_arrive_expect_tx(&s.kv_full, 2 * NB * kBoxBytes);
+      for (int cb = 0; cb < NB; ++cb) {
+        tma_load_3d(s.k[cb], &tk, &s.kv_full, cb * 64, c0, zkv);
+        tma_load_3d(s.v[cb], &tv, &s.kv_full, cb * 64, c0, zkv);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % kQStages;
+        const int use = it / kQStages;
+        if (use > 0 && !mbar_wait(&s.q_empty[st], (use - 1) & 1, abort_flag, kSiteQEmpty)) break;
+        const int g = it / n_qt;
+        const int q0 = (qt_lo + it % n_qt) * kTileM;
+        const int zq = b * p.Hq + hk * p.group + g;
+        mbar_arrive_expect_tx(&s.q_full[st], 2 * NB * kBoxBytes);
+        for (int cb = 0; cb < NB; ++cb) {
+          tma_load_3d(s.q[st][cb], &tq, &s.q_full[st], cb * 64, q0, zq);
+          tma_load_3d(s.dout[st][cb], &tdo, &s.q_full[st], cb * 64, q0, zq);
+        }
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        mbar_drain(&s.kv_full, 0, kSiteDrain);
+        for (int it = max(0, issued - kQStages); it < issued; ++it)
+          mbar_drain(&s.q_full[it % kQStages], (it / kQStages) & 1, kSiteDrain);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0 && n_it > 0) {
+      constexpr uint32_t id_kq = idesc_bf16_f32(kTileN, kTileM, false, false);  // S^T, dP^T
+      constexpr uint32_t id_acc = idesc_bf16_f32(kTileN, D, false, true);       // dV, dK
+      constexpr uint32_t id_dq = idesc_bf16_f32(kTileM, D, true, true);         // dQ
+      bool ok = mbar_wait(&s.kv_full, 0, abort_flag, kSiteKV);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % kQStages;
+        if (!mbar_wait(&s.q_full[st], (it / kQStages) & 1, abort_flag, kSiteQFull)) break;
+        tc_fence_after();
+        // S^T = K Q^T  (A = K rows, B = Q rows, both K-major over d)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(smem_u32(s.k[kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bq =
+              smem_desc_sw128(smem_u32(s.q[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          mma_ss(t_S, a, bq, id_kq, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s.s_full);
+        // dP^T = V dO^T; its columns held dQ of the previous tile
+        if (it > 0 && !mbar_wait(&s.dq_empty, (it - 1) & 1, abort_flag, kSiteDQEmpty)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(smem_u32(s.v[kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bo =
+              smem_desc_sw128(smem_u32(s.dout[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          mma_ss(t_dP, a, bo, id_kq, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s.dp_full);
+        // dV += P^T dO  (A = P^T in TMEM; B = dO rows, MN-major over d)
+        if (!mbar_wait(&s.p_full, it & 1, abort_flag, kSiteP)) break;
+        tc_fence_after();
+        {
+          const uint32_t o0 = smem_u32(s.dout[st][0]);
+          const uint32_t lbo = (NB > 1) ? (smem_u32(s.dout[st][NB - 1]) - o0) : 16u;
+#pragma unroll
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            mma_ts(t_dV, t_S + kk * 8, smem_desc_sw128(o0 + kk * 2048, lbo, 1024), id_acc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dK += dS^T Q  (A = dS^T in TMEM; B = Q rows, MN-major over d)
+        if (!mbar_wait(&s.ds_full, it & 1, abort_flag, kSiteDS)) break;
+        tc_fence_after();
+        {
+          const uint32_t q0a = smem_u32(s.q[st][0]);
+          const uint32_t lbo = (NB > 1) ? (smem_u32(s.q[st][NB - 1]) - q0a) : 16u;
+#pragma unroll
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            mma_ts(t_dK, t_dP + kk * 8, smem_desc_sw128(q0a + kk * 2048, lbo, 1024), id_acc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dQ = dS K  (A = dS: shared rows = keys, queries contiguous -> MN-major;
+        //             B = K rows, d contiguous -> MN-major), into the dP^T columns
+        {
+          const uint32_t ds0 = smem_u32(s.ds[0]);
+          const uint32_t lbo_a = smem_u32(s.ds[1]) - ds0;
+          const uint32_t k0 = smem_u32(s.k[0]);
+          const uint32_t lbo_b = (NB > 1) ? (smem_u32(s.k[NB - 1]) - k0) : 16u;
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ss(t_dP, smem_desc_sw128(ds0 + kk * 2048, lbo_a, 1024),
+                   smem_desc_sw128(k0 + kk * 2048, lbo_b, 1024), id_dq, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s.dq_full);
+        mma_commit(&s.q_empty[st]);
+      }
+      mma_commit(&s.dkv_full);
+      if (*abort_flag) {
+        mma_commit(&s.drain);
+        mbar_drain(&s.drain, 0, kSiteDrain);
+      }
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------- compute warps --
+    const int row = warp * 32 + lane;  // key row in the tile = TMEM lane
+    const int key = c0 + row;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const bool key_in = key >= klo && key < kend;
+    const float c = p.scale_log2;
+    const uint32_t ds_base = smem_u32(s.ds[0]);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int g = it / n_qt;
+      const int q0 = (qt_lo + it % n_qt) * kTileM;
+      const int h = hk * p.group + g;
+      // Row statistics of this query tile, staged in the buffer of this tile's
+      // parity.  Every compute thread has finished tile it-2 (the last reader
+      // of this buffer) before any thread can pass tile it-1's barrier.
+      const int sb = it & 1;
+      {
+        const int qi = q0 + row;
+        float l2 = pos_inf(), dd = 0.f;
+        if (qi < p.Sq) {
+          const size_t ri = (static_cast<size_t>(b) * p.Hq + h) * p.Sq + qi;
+          const float lse = p.lse[ri];
+          l2 = (lse == neg_inf()) ? pos_inf() : lse * 1.4426950408889634f;
+          dd = p.delta[ri];
+        }
+        s.lse2[sb][row] = l2;
+        s.delta[sb][row] = dd;
+      }
+      mbar_arrive(&s.stat_ready[sb]);
+      if (!mbar_wait_warp(&s.stat_ready[sb], (it >> 1) & 1, abort_flag, kSiteStat)) { ok = false; break; }
+      const float* lse2 = s.lse2[sb];
+      const float* dlt = s.delta[sb];
+      // visible queries of this key row: q >= key - off (causal), key in [klo, kend)
+      const int qmin = p.causal ? key - off : -0x7fffffff;
+      const bool need_mask = !key_in || (p.causal && q0 < qmin);
+      if (!mbar_wait_warp(&s.s_full, it & 1, abort_flag, kSiteS)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pk[kTileM / 2];
+#pragma unroll
+      for (int cc = 0; cc < kTileM / 32; ++cc) {
+        uint32_t sr[32];
+        tmem_ld32(t_S + lane_off + cc * 32, sr);
+        tmem_wait_ld();
+        uint32_t pw[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int qa = cc * 32 + 2 * e;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * e]), c, -lse2[qa]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), c, -lse2[qa + 1]));
+          if (need_mask) {
+            if (!key_in || q0 + qa < qmin) p0 = 0.f;
+            if (!key_in || q0 + qa + 1 < qmin) p1 = 0.f;
+          }
+          pw[e] = pack_bf16x2(p0, p1);
+          pk[cc * 16 + e] = pw[e];
+        }
+        tmem_st16(t_S + lane_off + cc * 16, pw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.p_full);
+      // dS^T = P^T * (dP^T - D)
+      if (!mbar_wait_warp(&s.dp_full, it & 1, abort_flag, kSiteDP)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < kTileM / 32; ++cc) {
+        uint32_t dr[32];
+        tmem_ld32(t_dP + lane_off + cc * 32, dr);
+        tmem_wait_ld();
+        uint32_t dw[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int qa = cc * 32 + 2 * e;
+          const uint32_t w = pk[cc * 16 + e];
+          const float d0 = __uint_as_float(w << 16) * (__uint_as_float(dr[2 * e]) - dlt[qa]);
+          const float d1 =
+              __uint_as_float(w & 0xffff0000u) * (__uint_as_float(dr[2 * e + 1]) - dlt[qa + 1]);
+          dw[e] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(t_dP + lane_off + cc * 16, dw);
+        // shared copy: 32 queries = four 16-byte chunks of query block cc/2
+        const uint32_t blk = ds_base + (cc >> 1) * (kTileN * 128) + row * 128;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t chunk = static_cast<uint32_t>(((cc & 1) * 4 + ch) ^ (row & 7));
+          st_shared_v4(blk + chunk * 16, dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.ds_full);
+    }
+    // ---- epilogue: dK = scale * acc, dV = acc  (zeros when no query sees the keys)
+    if (ok && n_it > 0) ok = mbar_wait_warp(&s.dkv_full, 0, abort_flag, kSiteDKV);
+    tc_fence_after();
+    // warp-uniform: the TMEM loads below are warp-collective, only the stores
+    // depend on the lane's key
+    if (ok && !warp_aborted(abort_flag)) {
+      const bool store = key < p.Sk;
+      const size_t kr = (static_cast<size_t>(b) * p.Hkv + hk) * p.Sk + key;
+      __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
+      __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        const uint32_t src = (pass == 0) ? t_dK : t_dV;
+        const float mul = (pass == 0) ? p.scale : 1.f;
+        __nv_bfloat16* dst = (pass == 0) ? dkrow : dvrow;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          if (n_it > 0) {
+            tmem_ld32(src + lane_off + cc * 32, r);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = 0u;
+          }
+          uint32_t pw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pw[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+          if (store) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              d4[e] = make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------- dQ drain (warps 4-7) --
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // query row in the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    for (int it = 0; it < n_it; ++it) {
+      const int g = it / n_qt;
+      const int q0 = (qt_lo + it % n_qt) * kTileM;
+      const int h = hk * p.group + g;
+      if (!mbar_wait_warp(&s.dq_full, it & 1, abort_flag, kSiteDQFull)) break;
+      tc_fence_after();
+      const int qi = q0 + row;
+      float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.Hq + h) * p.Sq + qi) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(t_dP + lane_off + cc * 32, r);
+        tmem_wait_ld();
+        if (qi < p.Sq) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(r[4 * e]),
+                       __uint_as_float(r[4 * e + 1]), __uint_as_float(r[4 * e + 2]),
+                       __uint_as_float(r[4 * e + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.dq_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  constexpr size_t smem = sizeof(BwdSmem<D>);
+  static_assert(smem <= 232448, "backward shared memory exceeds the per-CTA limit");
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
+  const long long pre_threads = rows * (D / 8);
+  fa_bwd_pre<D><<<static_cast<unsigned int>((pre_threads + 255) / 256), 256, 0, stream>>>(p, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int n_kt = (p.Sk + kTileN - 1) / kTileN;
+  const unsigned int grid = static_cast<unsigned int>(n_kt) * p.B * p.Hkv;
+  fa_bwd_main<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long n4 = rows * D / 4;
+  fa_bwd_convert<<<static_cast<unsigned int>((n4 + 255) / 256), 256, 0, stream>>>(p, n4);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, p, stream);
+  return launch_bwd_d<64>(tq, tk, tv, tdo, p, stream);
+}
+
 unsigned int read_bwd_status(bool clear) {
   unsigned int v = 0;
   cudaMemcpyFromSymbol(&v, g_status, sizeof v);
@@ -18,4 +515,5 @@ unsigned int read_bwd_status(bool clear) {
   }
   return v;
 }
+
 }  // namespace fa

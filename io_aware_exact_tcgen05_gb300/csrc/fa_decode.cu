@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int st = 0; st < n_stages; ++st) {
       const int slot = st % kStages;
-      if (!mbar_wait(&s.full[slot], (st / kStages) & 1, abort_flag, kSiteFull)) break;
+      if (!mbar_wait_warp(&s.full[slot], (st / kStages) & 1, abort_flag, kSiteFull)) break;
       const int stage_keys = min(kStageKeys, n_keys - st * kStageKeys);
       float sc[ROUNDS];
       uint4 vraw[ROUNDS];

@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = (t == 0) || active1;
     if (ok && n_tiles > 0) {
       for (int j = 0; j < n_tiles; ++j) {
-        if (!mbar_wait(&s.s_full[t], j & 1, abort_flag, kSiteSFull)) { ok = false; break; }
+        if (!mbar_wait_warp(&s.s_full[t], j & 1, abort_flag, kSiteSFull)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[kTileN];
 #pragma unroll
@@ -331,11 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&s.p_full[t]);
       }
-      if (ok) ok = mbar_wait(&s.o_full[t], 0, abort_flag, kSiteOFull);
+      if (ok) ok = mbar_wait_warp(&s.o_full[t], 0, abort_flag, kSiteOFull);
       tc_fence_after();
     }
     // ---- epilogue: O = u / l, LSE = m*scale + ln l ---------------------
-    if (((t == 0) || active1) && !*abort_flag) {
+    if (((t == 0) || active1) && ok && !warp_aborted(abort_flag)) {
       const bool live = l > 0.f;
       const float inv = live ? 1.f / lr : 0.f;
       const bool in_range = i < p.Sq;

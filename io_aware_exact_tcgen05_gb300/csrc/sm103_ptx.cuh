@@ -22,6 +22,7 @@ namespace fa {
 static __device__ unsigned int g_status = 0;
 
 constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
+constexpr uint32_t kWaitMaxSpins = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -82,12 +83,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
-    if ((++spins & 255u) == 0u && global_timer_ns() - t0 > kWaitTimeoutNs) {
+    ++spins;
+    // time limit, with a spin-count backstop that holds even if the timer stalls
+    if (((spins & 255u) == 0u && global_timer_ns() - t0 > kWaitTimeoutNs) ||
+        spins > kWaitMaxSpins) {
       raise_status(1u, site);
       *abort_flag = 1;
       return false;
     }
   }
+}
+
+// Warp-uniform wait for warps that go on to warp-collective instructions
+// (tcgen05.ld/st, shuffles): every lane waits, and the warp proceeds only if all
+// lanes succeeded.  The vote also reconverges the warp, which the .sync.aligned
+// TMEM instructions require.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag, unsigned int site) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// True on every lane when any lane of the warp sees the CTA's abort flag raised.
+__device__ __forceinline__ bool warp_aborted(volatile int* abort_flag) {
+  return __any_sync(0xffffffffu, *abort_flag != 0);
 }
 
 // Teardown wait after an abort: bounded like mbar_wait but it does not give up
@@ -98,7 +117,9 @@ __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, unsig
   const unsigned long long t0 = global_timer_ns();
   uint32_t spins = 0;
   while (!mbar_try_wait(a, parity)) {
-    if ((++spins & 255u) == 0u && global_timer_ns() - t0 > kWaitTimeoutNs) {
+    ++spins;
+    if (((spins & 255u) == 0u && global_timer_ns() - t0 > kWaitTimeoutNs) ||
+        spins > kWaitMaxSpins) {
       raise_status(1u, site);
       return false;
     }
