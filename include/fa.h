@@ -129,6 +129,16 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
    clear != 0 the words are reset to 0 afterwards. */
 fa_status fa_device_status(unsigned int* code_out, int clear);
 
+/* Profiling hook (the pages ask that a timing confirm which kernel actually
+   ran).  start/stop are cudaEvent_t handles created by the caller.  The next
+   fa_fwd, fa_bwd or fa_decode call made on this host thread records `start`
+   on its stream right before its main kernel (fa_fwd: the attention kernel;
+   fa_bwd: the key-tile kernel, not the preprocess or dQ-convert kernels;
+   fa_decode: the split partial kernel, not the merge) and `stop` right after
+   it, then the hook disarms itself.  Passing NULL for both disarms it.  The
+   events are not owned by the library. */
+fa_status fa_profile_next_launch(cudaEvent_t start, cudaEvent_t stop);
+
 /* Static text for a status code. */
 const char* fa_status_string(fa_status s);
 

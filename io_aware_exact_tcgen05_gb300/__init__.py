@@ -25,7 +25,8 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_decode", "fa_decode_workspace_size",
-            "fa_device_status", "fa_status_string", "fa_last_error_detail", "fa_version")
+            "fa_device_status", "fa_profile_next_launch", "fa_status_string",
+            "fa_last_error_detail", "fa_version")
 
 _lib = None
 
@@ -55,6 +56,8 @@ def load_library(path: str = LIB_PATH):
     lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
     for f in (lib.fa_fwd, lib.fa_bwd, lib.fa_decode, lib.fa_device_status):
         f.restype = I
+    lib.fa_profile_next_launch.argtypes = [P, P]
+    lib.fa_profile_next_launch.restype = I
     lib.fa_status_string.argtypes = [I]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_error_detail.restype = ctypes.c_char_p
@@ -172,6 +175,15 @@ def fa_device_status(clear: bool = True):
     w = ctypes.c_uint(0)
     st = lib.fa_device_status(ctypes.byref(w), int(bool(clear)))
     return st, w.value
+
+
+def fa_profile_next_launch(start=None, stop=None):
+    """Arm the one-shot hook: the next fa_* call on this thread records the two
+    torch.cuda.Event objects around its main kernel (None, None disarms)."""
+    lib = load_library()
+    a = None if start is None else ctypes.c_void_p(start.cuda_event)
+    b = None if stop is None else ctypes.c_void_p(stop.cuda_event)
+    _check(lib.fa_profile_next_launch(a, b), "fa_profile_next_launch")
 
 
 def version() -> str:

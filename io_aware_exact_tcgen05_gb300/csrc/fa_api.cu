@@ -15,9 +15,17 @@
 #include "../../include/fa.h"
 #include "fa_internal.h"
 
+namespace fa {
+ProfileHook& profile_hook() {
+  static thread_local ProfileHook h;
+  return h;
+}
+}  // namespace fa
+
 namespace {
 
 thread_local char g_detail[256] = "";
+
 
 fa_status fail(fa_status s, const char* fmt, ...) {
   va_list ap;
@@ -301,6 +309,14 @@ fa_status fa_device_status(unsigned int* code_out, int clear) {
                          fa::read_bwd_status(clear != 0);
   if (code_out) *code_out = w;
   if (w != 0) return fail(FA_ERR_TIMEOUT, "device status word 0x%08x", w);
+  return ok();
+}
+
+fa_status fa_profile_next_launch(cudaEvent_t start, cudaEvent_t stop) {
+  if ((start == nullptr) != (stop == nullptr))
+    return fail(FA_ERR_INVALID_ARG, "pass both events or neither");
+  fa::profile_hook().start = start;
+  fa::profile_hook().stop = stop;
   return ok();
 }
 

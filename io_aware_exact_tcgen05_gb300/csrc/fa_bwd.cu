@@ -490,7 +490,9 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   const int n_kt = (p.Sk + kTileN - 1) / kTileN;
   const unsigned int grid = static_cast<unsigned int>(n_kt) * p.B * p.Hkv;
+  hook_before(stream);
   fa_bwd_main<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  hook_after(stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long n4 = rows * D / 4;

@@ -395,7 +395,9 @@ cudaError_t launch_partial(const DecodeParams& p, int heads_per_cta, cudaStream_
   }
   const int n_hsub = (p.group + heads_per_cta - 1) / heads_per_cta;
   dim3 grid(p.n_split, p.Hkv * n_hsub, p.B);
+  hook_before(stream);
   fa_decode_partial<D, HG><<<grid, kThreads, smem, stream>>>(p, heads_per_cta);
+  hook_after(stream);
   return cudaGetLastError();
 }
 

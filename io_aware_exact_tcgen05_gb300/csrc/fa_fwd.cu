@@ -389,7 +389,9 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     configured = true;
   }
   const unsigned int grid = static_cast<unsigned int>(p.n_rbu) * p.units_per_rbu;
+  hook_before(stream);
   fa_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  hook_after(stream);
   return cudaGetLastError();
 }
 

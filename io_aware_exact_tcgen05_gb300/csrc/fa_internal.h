@@ -10,6 +10,22 @@
 
 namespace fa {
 
+// One-shot profiling events armed by fa_profile_next_launch (per host thread):
+// the launch helpers record `start` right before and `stop` right after the
+// main kernel of the next call, then clear them.
+struct ProfileHook {
+  cudaEvent_t start = nullptr;
+  cudaEvent_t stop = nullptr;
+};
+ProfileHook& profile_hook();
+inline void hook_before(cudaStream_t s) {
+  if (profile_hook().start) cudaEventRecord(profile_hook().start, s);
+}
+inline void hook_after(cudaStream_t s) {
+  if (profile_hook().stop) cudaEventRecord(profile_hook().stop, s);
+  profile_hook() = ProfileHook{};
+}
+
 // Rows of one query tile and keys of one key/value tile in the tensor-core
 // kernels (one tcgen05.mma M=128 accumulator; 128 TMEM lanes).
 constexpr int kTileM = 128;
