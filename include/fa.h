@@ -123,6 +123,36 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
                     int d, float scale, void* workspace, size_t workspace_bytes,
                     cudaStream_t stream);
 
+/* Size of the scratch array built into the library for fa_decode_noalloc. */
+#define FA_DECODE_NOALLOC_MAX_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * fa_decode without a workspace argument, for callers that cannot allocate
+ * device memory: callers whose interface only carries the input and output
+ * buffers (a fixed operator or plugin signature with no workspace slot), and
+ * callers that run where allocating is not possible or not wanted (a host
+ * framework that owns all device memory through its own pool, or a
+ * latency-critical loop that cannot pay for cudaMalloc and the device
+ * synchronisation it implies).  The pages have no counterpart: it is an
+ * interface variant of fa_decode, with the same arguments, results and errors
+ * minus workspace/workspace_bytes.
+ *
+ * Scratch comes from one array of FA_DECODE_NOALLOC_MAX_SCRATCH_BYTES (64 MiB)
+ * compiled into the library; each GPU on which it is used keeps that array
+ * until the process exits.  No device memory is allocated by the call.
+ *   - Problems whose fa_decode_workspace_size(B, Hq, Sk_max, d) exceeds the
+ *     array are rejected with FA_ERR_WORKSPACE before any device work.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the array: calls that can overlap on the GPU
+ *     (different streams without ordering between them) race and corrupt each
+ *     other's results.  Calls ordered on one stream are safe; nothing in the
+ *     array needs to start at zero.
+ */
+fa_status fa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,
+                            float* lse, const int32_t* seqlens_k, int B, int Hq, int Hkv,
+                            int Sk_max, int d, float scale, cudaStream_t stream);
+
 /* Reads the device status words of the current device (this synchronises the
    device).  Returns FA_OK or FA_ERR_TIMEOUT; *code_out (may be NULL) receives
    the raw word (low 16 bits: error code, high 16 bits: wait site).  When

@@ -25,7 +25,8 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_decode", "fa_decode_workspace_size",
-            "fa_device_status", "fa_profile_next_launch", "fa_status_string",
+            "fa_decode_noalloc", "fa_device_status", "fa_profile_next_launch",
+            "fa_status_string",
             "fa_last_error_detail", "fa_version")
 
 _lib = None
@@ -49,6 +50,8 @@ def load_library(path: str = LIB_PATH):
     lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P]
     lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, Z, P]
     lib.fa_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P, Z, P]
+    lib.fa_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
+    lib.fa_decode_noalloc.restype = I
     lib.fa_bwd_workspace_size.argtypes = [I, I, I, I]
     lib.fa_bwd_workspace_size.restype = Z
     lib.fa_decode_workspace_size.argtypes = [I, I, I, I]
@@ -166,6 +169,30 @@ def fa_decode(q, k_cache, v_cache, seqlens_k, scale: float, o=None, lse=None, wo
                        _ptr(seqlens_k), B, Hq, Hkv, Sk_max, d, float(scale), _ptr(workspace),
                        workspace.numel(), _stream(stream))
     _check(st, "fa_decode")
+    return o, lse
+
+
+DECODE_NOALLOC_MAX_SCRATCH_BYTES = 64 << 20
+
+
+def fa_decode_noalloc(q, k_cache, v_cache, seqlens_k, scale: float, o=None, lse=None,
+                      stream=None):
+    """fa_decode without a caller workspace: the library uses its built-in
+    64 MiB scratch array instead (see include/fa.h).  For callers that cannot
+    allocate device scratch; outputs may still be passed in.  Calls that can
+    overlap on the GPU share that scratch and race."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(seqlens_k, "seqlens_k", torch.int32, 1)
+    B, Hq, _, d = q.shape
+    _, Hkv, Sk_max, _ = k_cache.shape
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device) if lse is None else lse
+    st = lib.fa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
+                               _ptr(seqlens_k), B, Hq, Hkv, Sk_max, d, float(scale),
+                               _stream(stream))
+    _check(st, "fa_decode_noalloc")
     return o, lse
 
 

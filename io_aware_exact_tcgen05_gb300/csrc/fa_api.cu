@@ -26,6 +26,14 @@ namespace {
 
 thread_local char g_detail[256] = "";
 
+}  // namespace
+
+namespace fa {
+// Lets other translation units report a detail through fa_last_error_detail.
+void set_error_detail(const char* text) { snprintf(g_detail, sizeof g_detail, "%s", text); }
+}  // namespace fa
+
+namespace {
 
 fa_status fail(fa_status s, const char* fmt, ...) {
   va_list ap;
