@@ -165,15 +165,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.q_empty[i], 1);
     }
     mbar_init(&s.s_full, 1);
-    mbar_init(&s.p_full, 128);
+    mbar_init(&s.p_full, 4);  // one arrival per compute warp
     mbar_init(&s.dp_full, 1);
-    mbar_init(&s.ds_full, 128);
+    mbar_init(&s.ds_full, 4);
     mbar_init(&s.dq_full, 1);
-    mbar_init(&s.dq_empty, 128);
+    mbar_init(&s.dq_empty, 4);  // one arrival per drain warp
     mbar_init(&s.dkv_full, 1);
     mbar_init(&s.drain, 1);
-    mbar_init(&s.stat_ready[0], 128);
-    mbar_init(&s.stat_ready[1], 128);
+    mbar_init(&s.stat_ready[0], 4);
+    mbar_init(&s.stat_ready[1], 4);
     s.abort_flag = 0;
     fence_barrier_init();
   }
@@ -231,18 +231,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_kq = idesc_bf16_f32(kTileN, kTileM, false, false);  // S^T, dP^T
       constexpr uint32_t id_acc = idesc_bf16_f32(kTileN, D, false, true);       // dV, dK
       constexpr uint32_t id_dq = idesc_bf16_f32(kTileM, D, true, true);         // dQ
+      // Descriptors are built once; each MMA adds a compile-time offset.
+      constexpr uint32_t kStage = NB * kBoxBytes;
+      constexpr uint32_t kLbo = NB > 1 ? kBoxBytes : 16u;  // next 64-wide d block
+      const uint64_t k_kmaj = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
+      const uint64_t v_kmaj = smem_desc_sw128(smem_u32(s.v[0]), 16, 1024);
+      const uint64_t k_mn = smem_desc_sw128(smem_u32(s.k[0]), kLbo, 1024);
+      const uint64_t q_kmaj0 = smem_desc_sw128(smem_u32(s.q[0][0]), 16, 1024);
+      const uint64_t o_kmaj0 = smem_desc_sw128(smem_u32(s.dout[0][0]), 16, 1024);
+      const uint64_t q_mn0 = smem_desc_sw128(smem_u32(s.q[0][0]), kLbo, 1024);
+      const uint64_t o_mn0 = smem_desc_sw128(smem_u32(s.dout[0][0]), kLbo, 1024);
+      const uint64_t ds_mn = smem_desc_sw128(smem_u32(s.ds[0]), kBoxBytes, 1024);
       bool ok = mbar_wait(&s.kv_full, 0, abort_flag, kSiteKV);
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % kQStages;
+        const uint32_t so = static_cast<uint32_t>(st) * kStage;
         if (!mbar_wait(&s.q_full[st], (it / kQStages) & 1, abort_flag, kSiteQFull)) break;
         tc_fence_after();
         // S^T = K Q^T  (A = K rows, B = Q rows, both K-major over d)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(smem_u32(s.k[kk >> 2]) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bq =
-              smem_desc_sw128(smem_u32(s.q[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
-          mma_ss(t_S, a, bq, id_kq, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(t_S, desc_add(k_kmaj, off), desc_add(q_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s.s_full);
         // dP^T = V dO^T; its columns held dQ of the previous tile
@@ -250,46 +260,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(smem_u32(s.v[kk >> 2]) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bo =
-              smem_desc_sw128(smem_u32(s.dout[st][kk >> 2]) + (kk & 3) * 32, 16, 1024);
-          mma_ss(t_dP, a, bo, id_kq, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(t_dP, desc_add(v_kmaj, off), desc_add(o_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s.dp_full);
         // dV += P^T dO  (A = P^T in TMEM; B = dO rows, MN-major over d)
         if (!mbar_wait(&s.p_full, it & 1, abort_flag, kSiteP)) break;
         tc_fence_after();
-        {
-          const uint32_t o0 = smem_u32(s.dout[st][0]);
-          const uint32_t lbo = (NB > 1) ? (smem_u32(s.dout[st][NB - 1]) - o0) : 16u;
+        mma_ts(t_dV, t_S, desc_add(o_mn0, so), id_acc, it > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ts(t_dV, t_S + kk * 8, smem_desc_sw128(o0 + kk * 2048, lbo, 1024), id_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kTileM / 16; ++kk)
+          mma_ts(t_dV, t_S + kk * 8, desc_add(o_mn0, so + kk * 2048), id_acc, 1u);
         // dK += dS^T Q  (A = dS^T in TMEM; B = Q rows, MN-major over d)
         if (!mbar_wait(&s.ds_full, it & 1, abort_flag, kSiteDS)) break;
         tc_fence_after();
-        {
-          const uint32_t q0a = smem_u32(s.q[st][0]);
-          const uint32_t lbo = (NB > 1) ? (smem_u32(s.q[st][NB - 1]) - q0a) : 16u;
+        mma_ts(t_dK, t_dP, desc_add(q_mn0, so), id_acc, it > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ts(t_dK, t_dP + kk * 8, smem_desc_sw128(q0a + kk * 2048, lbo, 1024), id_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kTileM / 16; ++kk)
+          mma_ts(t_dK, t_dP + kk * 8, desc_add(q_mn0, so + kk * 2048), id_acc, 1u);
         // dQ = dS K  (A = dS: shared rows = keys, queries contiguous -> MN-major;
         //             B = K rows, d contiguous -> MN-major), into the dP^T columns
-        {
-          const uint32_t ds0 = smem_u32(s.ds[0]);
-          const uint32_t lbo_a = smem_u32(s.ds[1]) - ds0;
-          const uint32_t k0 = smem_u32(s.k[0]);
-          const uint32_t lbo_b = (NB > 1) ? (smem_u32(s.k[NB - 1]) - k0) : 16u;
 #pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk)
-            mma_ss(t_dP, smem_desc_sw128(ds0 + kk * 2048, lbo_a, 1024),
-                   smem_desc_sw128(k0 + kk * 2048, lbo_b, 1024), id_dq, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ss(t_dP, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), id_dq,
+                 kk > 0 ? 1u : 0u);
         mma_commit(&s.dq_full);
         mma_commit(&s.q_empty[st]);
       }
@@ -328,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         s.lse2[sb][row] = l2;
         s.delta[sb][row] = dd;
       }
-      mbar_arrive(&s.stat_ready[sb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.stat_ready[sb]);
       if (!mbar_wait_warp(&s.stat_ready[sb], (it >> 1) & 1, abort_flag, kSiteStat)) { ok = false; break; }
       const float* lse2 = s.lse2[sb];
       const float* dlt = s.delta[sb];
@@ -360,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&s.p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.p_full);
       // dS^T = P^T * (dP^T - D)
       if (!mbar_wait_warp(&s.dp_full, it & 1, abort_flag, kSiteDP)) { ok = false; break; }
       tc_fence_after();
@@ -391,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&s.ds_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.ds_full);
     }
     // ---- epilogue: dK = scale * acc, dV = acc  (zeros when no query sees the keys)
     if (ok && n_it > 0) ok = mbar_wait_warp(&s.dkv_full, 0, abort_flag, kSiteDKV);
@@ -458,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&s.dq_empty);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.dq_empty);
     }
   }
 

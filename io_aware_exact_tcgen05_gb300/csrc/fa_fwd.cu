@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s.s_full[t], 1);
-      mbar_init(&s.p_full[t], 4 * 32);
+      mbar_init(&s.p_full[t], 4);  // one arrival per softmax warp
       mbar_init(&s.o_full[t], 1);
     }
     mbar_init(&s.drain, 1);
@@ -144,7 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
-
   if (warp == 8) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0 && n_tiles > 0) {
@@ -189,6 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, false, true);
       const int nslots = active1 ? 2 : 1;
+      // Descriptors are built once; each MMA only adds a compile-time offset,
+      // so the issuing thread keeps up with the 64-cycle MMAs.
+      constexpr uint32_t kStage = NB * kBoxBytes;  // bytes per K (or V) stage
+      const uint64_t qd0 = smem_desc_sw128(smem_u32(s.q[0][0]), 16, 1024);
+      const uint64_t qd1 = smem_desc_sw128(smem_u32(s.q[1][0]), 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(smem_u32(s.k[0][0]), 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(smem_u32(s.v[0][0]), NB > 1 ? kBoxBytes : 16u, 1024);
       bool ok = mbar_wait(&s.bar_q, 0, abort_flag, kSiteQ);
       tc_fence_after();
       for (int j = 0; ok && j <= n_tiles; ++j) {
@@ -196,6 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&s.k_full[j % NS], (j / NS) & 1, abort_flag, kSiteKFull)) break;
           tc_fence_after();
         }
+        const uint64_t kd = desc_add(kd0, static_cast<uint32_t>(j % NS) * kStage);
+        const uint64_t vd = desc_add(vd0, static_cast<uint32_t>((j + NS - 1) % NS) * kStage);
         for (int t = 0; t < nslots; ++t) {
           const uint32_t t_s = tmem + t * kTileN;
           if (j > 0) {
@@ -208,24 +216,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t t_o = tmem + 2 * kTileN + t * D;
-            const uint32_t v0 = smem_u32(s.v[vs][0]);
-            const uint32_t lbo = (NB > 1) ? (smem_u32(s.v[vs][NB - 1]) - v0) : 16u;
+            mma_ts(t_o, t_s, vd, idesc_pv, j > 1 ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk) {
-              const uint64_t bdesc = smem_desc_sw128(v0 + kk * 16 * 128, lbo, 1024);
-              mma_ts(t_o, t_s + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 1; kk < kTileN / 16; ++kk)
+              mma_ts(t_o, t_s + kk * 8, desc_add(vd, kk * 16 * 128), idesc_pv, 1u);
           }
           if (j < n_tiles) {
             // S_t = Q_t K_j^T
-            const int ks = j % NS;
+            const uint64_t qd = t ? qd1 : qd0;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t adesc =
-                  smem_desc_sw128(smem_u32(s.q[t][kk >> 2]) + (kk & 3) * 32, 16, 1024);
-              const uint64_t bdesc =
-                  smem_desc_sw128(smem_u32(s.k[ks][kk >> 2]) + (kk & 3) * 32, 16, 1024);
-              mma_ss(t_s, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+              const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+              mma_ss(t_s, desc_add(qd, off), desc_add(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit(&s.s_full[t]);
           } else {
@@ -277,14 +279,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (key < klo || key >= khi_row) sr[jj] = 0xff800000u;
           }
         }
-        // row max with 8 independent chains (short dependency chains)
+        // row max: 8 independent chains of 3-input max
         float mx8[8];
 #pragma unroll
-        for (int q2 = 0; q2 < 8; ++q2) mx8[q2] = __uint_as_float(sr[q2]);
+        for (int q2 = 0; q2 < 8; ++q2)
+          mx8[q2] = fmaxf(__uint_as_float(sr[q2]), __uint_as_float(sr[q2 + 8]));
 #pragma unroll
-        for (int jj = 8; jj < kTileN; ++jj) mx8[jj & 7] = fmaxf(mx8[jj & 7], __uint_as_float(sr[jj]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int jj = 16; jj < kTileN; jj += 16)
+#pragma unroll
+          for (int q2 = 0; q2 < 8; ++q2)
+            mx8[q2] = max3f(mx8[q2], __uint_as_float(sr[jj + q2]), __uint_as_float(sr[jj + 8 + q2]));
+        const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
         const float m_new = fmaxf(m, mx);
         // (m_new - m) is NaN only when both are -inf: no rescale then.
         const bool grow = (m_new - m) * c > p.rescale_log2;
@@ -297,22 +303,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mc = (m == neg_inf()) ? 0.f : m * c;
         // l sums the fp32 weights (it gives the LSE); lr sums the bf16-rounded
         // weights the PV MMA actually multiplies, so O = u / lr is an exactly
-        // normalised combination of the V rows
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-        float sumr4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[kTileN / 2];
+        // normalised combination of the V rows.  Pairs go through the f32x2 pipes.
+        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t nmc2 = f2_pack(-mc, -mc);
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint64_t sumr2[4] = {0ull, 0ull, 0ull, 0ull};
+        // two halves of 64 scores; each half's P (32 packed columns) is stored
+        // as soon as it exists, into columns whose S values are already loaded
 #pragma unroll
-        for (int jj = 0; jj < kTileN / 2; ++jj) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * jj]), c, -mc));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * jj + 1]), c, -mc));
-          sum4[jj & 3] += p0 + p1;
-          pk[jj] = pack_bf16x2(p0, p1);
-          sumr4[jj & 3] += __uint_as_float(pk[jj] << 16) + __uint_as_float(pk[jj] & 0xffff0000u);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[kTileN / 4];
+#pragma unroll
+          for (int jq = 0; jq < kTileN / 4; ++jq) {
+            const int jj = half * (kTileN / 4) + jq;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * jj]), __uint_as_float(sr[2 * jj + 1])),
+                             c2, nmc2),
+                      x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            pk[jq] = pack_bf16x2(p0, p1);
+            sum2[jq & 3] = f2_add(sum2[jq & 3], f2_pack(p0, p1));
+            sumr2[jq & 3] = f2_add(sumr2[jq & 3], bf16x2_to_f2(pk[jq]));
+          }
+          tmem_st32(t_s + half * 32, pk);
         }
-        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-        lr += (sumr4[0] + sumr4[1]) + (sumr4[2] + sumr4[3]);
-        tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), a0, a1);
+          f2_unpack(f2_add(f2_add(sumr2[0], sumr2[1]), f2_add(sumr2[2], sumr2[3])), b0, b1);
+          l += a0 + a1;
+          lr += b0 + b1;
+        }
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
           // O_t is quiescent here: PV_t(j-1) completed before S_t(j) was
           // signalled, and PV_t(j) is issued only after p_full below.
@@ -329,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&s.p_full[t]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.p_full[t]);
       }
       if (ok) ok = mbar_wait_warp(&s.o_full[t], 0, abort_flag, kSiteOFull);
       tc_fence_after();
@@ -341,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool in_range = i < p.Sq;
       const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Sq + i;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
-#pragma unroll
+#pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t orr[32];
         if (n_tiles > 0) {
