@@ -9,7 +9,7 @@
 // Partial kernel: one CTA per (split, KV head, batch row) streams keys
 // [split*chunk, min((split+1)*chunk, seqlen)) of that KV head once and serves
 // all the query heads that read it (grouped heads).  Each of the 8 compute
-// warps takes 8 keys of every 64-key stage; a key row (d bf16) is spread over
+// warps takes 16 keys of every 128-key stage; a key row (d bf16) is spread over
 // d/8 lanes (8 values each), so one warp instruction covers 32*8/d keys.  The
 // per-key dot products with every query head are reduced across those lanes
 // with a transpose-reduce (each exchange halves the heads a lane carries), then
@@ -32,7 +32,7 @@ namespace {
 
 constexpr int kComputeWarps = 8;
 constexpr int kThreads = (kComputeWarps + 1) * 32;  // + 1 producer warp
-constexpr int kStageKeys = 64;
+constexpr int kStageKeys = 128;
 constexpr int kStages = 3;
 constexpr int kMaxHeadsPerCta = 8;
 
@@ -197,29 +197,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my_head = head_of<HG, LPK>(x);
     const float c = p.scale_log2;
     // query slices (fp32) for every head this CTA serves; padding heads are 0
-    float qv[HG][8];
+    // query slices and output accumulators as fp32 pairs for the f32x2 FMA pipe;
+    // padding heads get q = 0
+    uint64_t qv2[HG][4];
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
       if (h < n_heads) {
         const uint4 w = *reinterpret_cast<const uint4*>(
             reinterpret_cast<const __nv_bfloat16*>(p.q) +
             (static_cast<size_t>(b) * p.Hq + hq0 + h) * D + x * 8);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          qv[h][2 * e] = bf_lo(ww[e]);
-          qv[h][2 * e + 1] = bf_hi(ww[e]);
-        }
+        qv2[h][0] = bf16x2_to_f2(w.x);
+        qv2[h][1] = bf16x2_to_f2(w.y);
+        qv2[h][2] = bf16x2_to_f2(w.z);
+        qv2[h][3] = bf16x2_to_f2(w.w);
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qv[h][e] = 0.f;
+        for (int e = 0; e < 4; ++e) qv2[h][e] = 0ull;
       }
     }
-    float acc[HG][8];
+    uint64_t acc2[HG][4];
 #pragma unroll
     for (int h = 0; h < HG; ++h)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc2[h][e] = 0ull;
     float m = neg_inf();  // running max (raw score) of my_head over this warp's keys
     float l = 0.f;
 
@@ -233,9 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < ROUNDS; ++r) {
         const int key = warp * KPW + r * KPR + kr;
         const bool valid = key < stage_keys;
-        float part[HG];
-#pragma unroll
-        for (int h = 0; h < HG; ++h) part[h] = 0.f;
         uint4 kw = make_uint4(0u, 0u, 0u, 0u);
         vraw[r] = make_uint4(0u, 0u, 0u, 0u);
         if (valid) {
@@ -243,14 +240,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           vraw[r] = *reinterpret_cast<const uint4*>(&s.v[slot][key * D + x * 8]);
         }
         const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
+        uint64_t part2[HG];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) part2[h] = 0ull;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float k0 = bf_lo(kk[e]), k1 = bf_hi(kk[e]);
+          const uint64_t k2 = bf16x2_to_f2(kk[e]);
 #pragma unroll
-          for (int h = 0; h < HG; ++h) {
-            part[h] = fmaf(qv[h][2 * e], k0, part[h]);
-            part[h] = fmaf(qv[h][2 * e + 1], k1, part[h]);
-          }
+          for (int h = 0; h < HG; ++h) part2[h] = f2_fma(qv2[h][e], k2, part2[h]);
+        }
+        float part[HG];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          float lo, hi;
+          f2_unpack(part2[h], lo, hi);
+          part[h] = lo + hi;
         }
         const float sfull = transpose_reduce<HG, LPK>(part, lane);
         sc[r] = valid ? sfull : neg_inf();
@@ -270,8 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
           const float ah = __shfl_sync(0xffffffffu, alpha, lane_of_head<HG, LPK>(h));
+          const uint64_t ah2 = f2_pack(ah, ah);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] *= ah;
+          for (int e = 0; e < 4; ++e) acc2[h][e] = f2_mul(acc2[h][e], ah2);
         }
       }
       const float mc = (m == neg_inf()) ? 0.f : m * c;
@@ -288,24 +293,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- O_h += p_h(key) * v(key) ----
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
-        const uint32_t vv[4] = {vraw[r].x, vraw[r].y, vraw[r].z, vraw[r].w};
-        float vf[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          vf[2 * e] = bf_lo(vv[e]);
-          vf[2 * e + 1] = bf_hi(vv[e]);
-        }
+        const uint64_t v2[4] = {bf16x2_to_f2(vraw[r].x), bf16x2_to_f2(vraw[r].y),
+                                bf16x2_to_f2(vraw[r].z), bf16x2_to_f2(vraw[r].w)};
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
           const float ph =
               __shfl_sync(0xffffffffu, pr[r], (lane & ~(LPK - 1)) + lane_of_head<HG, LPK>(h));
+          const uint64_t ph2 = f2_pack(ph, ph);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(ph, vf[e], acc[h][e]);
+          for (int e = 0; e < 4; ++e) acc2[h][e] = f2_fma(ph2, v2[e], acc2[h][e]);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.empty[slot]);
     }
+    float acc[HG][8];
+#pragma unroll
+    for (int h = 0; h < HG; ++h)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f2_unpack(acc2[h][e], acc[h][2 * e], acc[h][2 * e + 1]);
     // ---- fold the key groups of the warp (lanes with equal x) ----
 #pragma unroll
     for (int o = LPK; o < 32; o <<= 1)
@@ -420,10 +426,12 @@ void decode_plan(int B, int Hq, int Hkv, int Sk_max, int* chunk, int* n_split) {
   (void)B;
   (void)Hq;
   (void)Hkv;
-  // 512 keys (256 KiB of K+V at d=128) per CTA keeps thousands of CTAs in
-  // flight for long caches; short caches use smaller chunks so that a row
-  // still spreads over several CTAs.  Multiple of the 64-key stage.
-  int c = 512;
+  // 4096 keys (2 MiB of K+V at d=128) per CTA: long streams per CTA amortise
+  // the start-up and the per-split merge (measured on GB300: 512-key chunks
+  // reached 4.1 TB/s, 4096-key chunks 6.1 TB/s); short caches use smaller
+  // chunks so that a row still spreads over several CTAs.  Multiple of the
+  // 128-key stage.
+  int c = 4096;
   while (c > kStageKeys && Sk_max <= 4 * c) c >>= 1;
   *chunk = c;
   *n_split = (Sk_max + c - 1) / c;

@@ -359,6 +359,12 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return r;
 }
 
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // The two bf16 halves of a packed word as an fp32 pair (exact).
 __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
   uint64_t r;

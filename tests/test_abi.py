@@ -72,7 +72,8 @@ def test_workspace_sizes(lib):
     assert n >= rows * 128 * 4 + rows * 4
     assert n <= rows * 128 * 4 + rows * 4 + 512
     m = fa.fa_decode_workspace_size(32, 32, 32768, 128)
-    assert m >= 32 * 32 * (32768 // 512) * 129 * 4
+    assert m >= 32 * 32 * (32768 // 4096) * 129 * 4  # 4096-key splits for long caches
+    assert m <= 32 * 32 * (32768 // 128) * 129 * 4 + 512
     assert fa.fa_decode_workspace_size(0, 1, 1, 128) == 0
 
 
