@@ -104,6 +104,25 @@ fa_status make_map(CUtensorMap* map, const void* base, long heads, long rows, in
   return FA_OK;
 }
 
+// [heads, rows, d] fp32 tensor (the backward's dQ accumulator), 32-row x
+// 32-column boxes (128 bytes wide), 128-byte swizzle; used as the target of
+// TMA reduce-add, which skips rows past the end of a head.
+fa_status make_map_acc(CUtensorMap* map, void* base, long heads, long rows, int d) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                           static_cast<cuuint64_t>(d) * 4 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (fp32) failed (%d)", (int)r);
+  return FA_OK;
+}
+
 fa_status check_sizes(int B, int Hq, int Hkv, int Sq, int Sk, int d) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1)
     return fail(FA_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d Hq=%d Hkv=%d Sq=%d Sk=%d)", B, Hq,
@@ -305,7 +324,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-  cudaError_t e = fa::launch_bwd(d, tq, tk, tv, tdo, p, stream);
+  CUtensorMap tdq;
+  FA_TRY(make_map_acc(&tdq, p.dq_acc, 1L * B * Hq, Sq, d));
+  cudaError_t e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, stream);
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "fa_bwd launch: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -15,7 +15,12 @@
 //        dK  += dS^T Q           (A = dS^T from TMEM)
 //        dQ   = dS K             (A = dS from shared memory, written into the
 //                                 dP^T columns, which are free by then)
-//        dQacc += dQ             fp32 vector atomics        [drain warps]
+//        dQacc += dQ             TMEM -> shared (this tile's Q and dO stage,
+//                                free once dK and dV have read it) -> TMA
+//                                reduce-add into the fp32 accumulator
+//                                                            [drain warps]
+//      The stage is refilled (two tiles later) only after the drain's reduces
+//      have read it, so the drain never delays the compute warps.
 //      At the end dK (times scale) and dV leave TMEM as bf16.  With grouped
 //      heads dK/dV already hold the sum over the group's query heads.
 //   3. fa_bwd_convert: dQ = bf16(scale * dQacc)
@@ -70,12 +75,6 @@ struct BwdSmem {
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 __device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -127,7 +126,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
   using Smem = BwdSmem<D>;
   constexpr int NB = Smem::NB;
   constexpr uint32_t kBoxBytes = Smem::kBox * 2;
@@ -162,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.kv_full, 1);
     for (int i = 0; i < kQStages; ++i) {
       mbar_init(&s.q_full[i], 1);
-      mbar_init(&s.q_empty[i], 1);
+      mbar_init(&s.q_empty[i], 1 + 4);  // MMA commit + the 4 dQ drain warps
     }
     mbar_init(&s.s_full, 1);
     mbar_init(&s.p_full, 4);  // one arrival per compute warp
@@ -430,34 +429,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------- dQ drain (warps 4-7) --
+    // Each warp moves its 32 query rows of dQ from TMEM into a 128*d-byte slice
+    // of this tile's Q/dO stage (32-column boxes, 128-byte swizzle; warps 0-1
+    // of the group use the Q buffer, 2-3 the dO buffer) and hands them to TMA
+    // reduce-add.  The stage is released to the producer once TMA has read it.
     const int wq = warp & 3;
-    const int row = wq * 32 + lane;  // query row in the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    constexpr int kSlice = 32 * D * 4;  // bytes of one warp's rows
     for (int it = 0; it < n_it; ++it) {
       const int g = it / n_qt;
       const int q0 = (qt_lo + it % n_qt) * kTileM;
       const int h = hk * p.group + g;
+      const int st = it % kQStages;
+      unsigned char* region = reinterpret_cast<unsigned char*>(
+                                  wq < 2 ? &s.q[st][0][0] : &s.dout[st][0][0]) +
+                              (wq & 1) * kSlice;
+      const uint32_t region_u32 = smem_u32(region);
       if (!mbar_wait_warp(&s.dq_full, it & 1, abort_flag, kSiteDQFull)) break;
       tc_fence_after();
-      const int qi = q0 + row;
-      float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.Hq + h) * p.Sq + qi) * D;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int bx = 0; bx < D / 32; ++bx) {
         uint32_t r[32];
-        tmem_ld32(t_dP + lane_off + cc * 32, r);
+        tmem_ld32(t_dP + lane_off + bx * 32, r);
         tmem_wait_ld();
-        if (qi < p.Sq) {
+        const uint32_t base = region_u32 + bx * 4096 + lane * 128;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            red_add_v4(dst + cc * 32 + 4 * e, __uint_as_float(r[4 * e]),
-                       __uint_as_float(r[4 * e + 1]), __uint_as_float(r[4 * e + 2]),
-                       __uint_as_float(r[4 * e + 3]));
-        }
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(base + ((ch ^ (lane & 7)) * 16), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2],
+                       r[4 * ch + 3]);
       }
+      // dQ is out of TMEM: dP^T of the next tile may reuse the columns
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.dq_empty);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx)
+          tma_reduce_add_3d(&tdq, region + bx * 4096, bx * 32, q0 + wq * 32, b * p.Hq + h);
+        bulk_commit_group();
+        bulk_wait_read0();
+        mbar_arrive(&s.q_empty[st]);
+      }
+      __syncwarp();
     }
+    if (lane == 0) bulk_wait0();  // reduces complete before the CTA leaves
   }
 
   tc_fence_before();
@@ -470,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                         cudaStream_t stream) {
   constexpr size_t smem = sizeof(BwdSmem<D>);
   static_assert(smem <= 232448, "backward shared memory exceeds the per-CTA limit");
   static bool configured = false;
@@ -489,7 +507,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const int n_kt = (p.Sk + kTileN - 1) / kTileN;
   const unsigned int grid = static_cast<unsigned int>(n_kt) * p.B * p.Hkv;
   hook_before(stream);
-  fa_bwd_main<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  fa_bwd_main<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, p);
   hook_after(stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -501,9 +519,10 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, p, stream);
-  return launch_bwd_d<64>(tq, tk, tv, tdo, p, stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                       cudaStream_t stream) {
+  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, p, stream);
+  return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, p, stream);
 }
 
 unsigned int read_bwd_status(bool clear) {

@@ -92,7 +92,8 @@ struct BwdParams {
 };
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                       const BwdParams& p,
                        cudaStream_t stream);
 unsigned int read_bwd_status(bool clear);
 

@@ -172,6 +172,32 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// 3-D tiled reduce-add of a shared-memory box into global memory (bulk
+// async-group completion).  Elements past the tensor's bounds are skipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
+                                                  int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until the bulk groups this thread committed have finished reading
+// their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until the bulk groups this thread committed have fully completed.
+__device__ __forceinline__ void bulk_wait0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA
 // stores, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
