@@ -62,8 +62,8 @@ struct BwdSmem {
   __nv_bfloat16 q[kQStages][NB][kBox];
   __nv_bfloat16 dout[kQStages][NB][kBox];
   __nv_bfloat16 ds[2][kBox];        // dS^T rows = keys, two 64-query blocks, 128B swizzle
-  float lse2[2][kTileM];            // LSE * log2(e), +inf for rows without keys
-  float delta[2][kTileM];           // D_i; both double-buffered by tile parity
+  float nlse2[2][kTileM];           // -LSE * log2(e), -inf for rows without keys
+  float ndelta[2][kTileM];          // -D_i; both double-buffered by tile parity
   uint64_t stat_ready[2];
   uint64_t kv_full;
   uint64_t q_full[kQStages], q_empty[kQStages];
@@ -73,7 +73,6 @@ struct BwdSmem {
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
-__device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -310,22 +309,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // of this buffer) before any thread can pass tile it-1's barrier.
       const int sb = it & 1;
       {
+        // stored negated so that p = 2^(s*c + nl) and dP - D = dP + nd are one
+        // packed FMA / add per pair; rows without keys get nl = -inf (p = 0)
         const int qi = q0 + row;
-        float l2 = pos_inf(), dd = 0.f;
+        float nl = neg_inf(), nd = 0.f;
         if (qi < p.Sq) {
           const size_t ri = (static_cast<size_t>(b) * p.Hq + h) * p.Sq + qi;
           const float lse = p.lse[ri];
-          l2 = (lse == neg_inf()) ? pos_inf() : lse * 1.4426950408889634f;
-          dd = p.delta[ri];
+          nl = (lse == neg_inf()) ? neg_inf() : -lse * 1.4426950408889634f;
+          nd = -p.delta[ri];
         }
-        s.lse2[sb][row] = l2;
-        s.delta[sb][row] = dd;
+        s.nlse2[sb][row] = nl;
+        s.ndelta[sb][row] = nd;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.stat_ready[sb]);
       if (!mbar_wait_warp(&s.stat_ready[sb], (it >> 1) & 1, abort_flag, kSiteStat)) { ok = false; break; }
-      const float* lse2 = s.lse2[sb];
-      const float* dlt = s.delta[sb];
+      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(s.nlse2[sb]);
+      const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(s.ndelta[sb]);
+      const uint64_t c2 = f2_pack(c, c);
       // visible queries of this key row: q >= key - off (causal), key in [klo, kend)
       const int qmin = p.causal ? key - off : -0x7fffffff;
       const bool need_mask = !key_in || (p.causal && q0 < qmin);
@@ -341,8 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int qa = cc * 32 + 2 * e;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * e]), c, -lse2[qa]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), c, -lse2[qa + 1]));
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), c2,
+                           nl2[qa >> 1]),
+                    x0, x1);
+          float p0 = ex2_approx(x0);
+          float p1 = ex2_approx(x1);
           if (need_mask) {
             if (!key_in || q0 + qa < qmin) p0 = 0.f;
             if (!key_in || q0 + qa + 1 < qmin) p1 = 0.f;
@@ -368,10 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int qa = cc * 32 + 2 * e;
-          const uint32_t w = pk[cc * 16 + e];
-          const float d0 = __uint_as_float(w << 16) * (__uint_as_float(dr[2 * e]) - dlt[qa]);
-          const float d1 =
-              __uint_as_float(w & 0xffff0000u) * (__uint_as_float(dr[2 * e + 1]) - dlt[qa + 1]);
+          const uint64_t dp2 =
+              f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
+                     nd2[qa >> 1]);
+          float d0, d1;
+          f2_unpack(f2_mul(bf16x2_to_f2(pk[cc * 16 + e]), dp2), d0, d1);
           dw[e] = pack_bf16x2(d0, d1);
         }
         tmem_st16(t_dP + lane_off + cc * 16, dw);
