@@ -468,7 +468,7 @@ def run_only(args):
     dev = torch.device("cuda", 0)
     n = args.warmup + args.steps
     if args.only == "decode":
-        w = workloads.make(DECODE)
+        w = workloads.make(DECODE, **({"B": args.decode_batch} if args.decode_batch else {}))
         t = w.tensors
         q, kc, vc, sl = (t[x].to(dev) for x in ("q", "k", "v", "seqlens_k"))
         for _ in range(n):
@@ -499,6 +499,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", choices=["fwd", "bwd", "decode"], default=None)
+    ap.add_argument("--decode-batch", type=int, default=0,
+                    help="with --only decode: fewer sequences (a smaller profiling case)")
     args = ap.parse_args()
     if args.only:
         return run_only(args)
