@@ -31,9 +31,10 @@
 // section (masked probabilities and their score gradients are 0); the same
 // mask, statistics and scale as the forward.
 //
-// Warp roles (320 threads): warps 0-3 compute (one key row = one TMEM lane per
-// thread), warps 4-7 drain dQ (one query row per thread), warp 8 TMA producer,
-// warp 9 MMA issuer and TMEM owner.
+// Warp roles (448 threads): warps 0-7 compute (one key row = one TMEM lane per
+// thread; warps w and w+4 share the lanes of group w and split the 128 query
+// columns, so P and dS need no cross-warp exchange), warps 8-11 drain dQ (one
+// query row per thread), warp 12 TMA producer, warp 13 MMA issuer and TMEM owner.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -44,7 +45,11 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+// Warp roles: 0-7 compute (lane group warp&3, query-column half warp>>2),
+// 8-11 dQ drain, 12 TMA producer, 13 MMA issuer and TMEM owner.
+constexpr int kThreads = 448;
+constexpr int kWarpProducer = 12;
+constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kQStages = 2;
 
@@ -163,9 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.q_empty[i], 1 + 4);  // MMA commit + the 4 dQ drain warps
     }
     mbar_init(&s.s_full, 1);
-    mbar_init(&s.p_full, 4);  // one arrival per compute warp
+    mbar_init(&s.p_full, 8);  // one arrival per compute warp
     mbar_init(&s.dp_full, 1);
-    mbar_init(&s.ds_full, 4);
+    mbar_init(&s.ds_full, 8);
     mbar_init(&s.dq_full, 1);
     mbar_init(&s.dq_empty, 4);  // one arrival per drain warp
     mbar_init(&s.dkv_full, 1);
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(&s.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -183,13 +188,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
-  const uint32_t t_S = tmem;              // S^T, then P^T (bf16, first 64 columns)
-  const uint32_t t_dP = tmem + kTileN;    // dP^T, then dS^T (bf16), then dQ
+  // P^T (bf16) of query half hf sits in S^T columns [64 hf, 64 hf + 32) and
+  // dS^T in dP^T columns [64 hf, 64 hf + 32): inside the columns that half's
+  // own warps read, so neither half overwrites scores the other still needs.
+  const uint32_t t_S = tmem;              // S^T, then P^T
+  const uint32_t t_dP = tmem + kTileN;    // dP^T, then dS^T, then dQ
   const uint32_t t_dV = tmem + 2 * kTileN;
   const uint32_t t_dK = tmem + 2 * kTileN + D;
   volatile int* abort_flag = &s.abort_flag;
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0 && n_it > 0) {
       tma_prefetch_desc(&tq);
@@ -223,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_drain(&s.q_full[it % kQStages], (it / kQStages) & 1, kSiteDrain);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0 && n_it > 0) {
       constexpr uint32_t id_kq = idesc_bf16_f32(kTileN, kTileM, false, false);  // S^T, dP^T
@@ -268,14 +276,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ts(t_dV, t_S, desc_add(o_mn0, so), id_acc, it > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 1; kk < kTileM / 16; ++kk)
-          mma_ts(t_dV, t_S + kk * 8, desc_add(o_mn0, so + kk * 2048), id_acc, 1u);
+          mma_ts(t_dV, t_S + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(o_mn0, so + kk * 2048),
+                 id_acc, 1u);
         // dK += dS^T Q  (A = dS^T in TMEM; B = Q rows, MN-major over d)
         if (!mbar_wait(&s.ds_full, it & 1, abort_flag, kSiteDS)) break;
         tc_fence_after();
         mma_ts(t_dK, t_dP, desc_add(q_mn0, so), id_acc, it > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 1; kk < kTileM / 16; ++kk)
-          mma_ts(t_dK, t_dP + kk * 8, desc_add(q_mn0, so + kk * 2048), id_acc, 1u);
+          mma_ts(t_dK, t_dP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(q_mn0, so + kk * 2048),
+                 id_acc, 1u);
         // dQ = dS K  (A = dS: shared rows = keys, queries contiguous -> MN-major;
         //             B = K rows, d contiguous -> MN-major), into the dP^T columns
 #pragma unroll
@@ -291,11 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(&s.drain, 0, kSiteDrain);
       }
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ---------------------------------------------------- compute warps --
-    const int row = warp * 32 + lane;  // key row in the tile = TMEM lane
+    const int grp = warp & 3;           // TMEM lane group
+    const int hf = warp >> 2;           // query columns [64 hf, 64 hf + 64)
+    const int row = grp * 32 + lane;    // key row in the tile = TMEM lane
     const int key = c0 + row;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(grp * 32) << 16;
     const bool key_in = key >= klo && key < kend;
     const float c = p.scale_log2;
     const uint32_t ds_base = smem_u32(s.ds[0]);
@@ -304,11 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = it / n_qt;
       const int q0 = (qt_lo + it % n_qt) * kTileM;
       const int h = hk * p.group + g;
-      // Row statistics of this query tile, staged in the buffer of this tile's
-      // parity.  Every compute thread has finished tile it-2 (the last reader
-      // of this buffer) before any thread can pass tile it-1's barrier.
+      // Row statistics of this query tile, staged by the hf = 0 warps in the
+      // buffer of this tile's parity.  A buffer is rewritten two tiles later,
+      // after every compute warp has signalled dS of the tile that read it
+      // (S^T of the next tile is issued only after that).
       const int sb = it & 1;
-      {
+      if (hf == 0) {
         // stored negated so that p = 2^(s*c + nl) and dP - D = dP + nd are one
         // packed FMA / add per pair; rows without keys get nl = -inf (p = 0)
         const int qi = q0 + row;
@@ -321,28 +334,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         s.nlse2[sb][row] = nl;
         s.ndelta[sb][row] = nd;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.stat_ready[sb]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.stat_ready[sb]);
       if (!mbar_wait_warp(&s.stat_ready[sb], (it >> 1) & 1, abort_flag, kSiteStat)) { ok = false; break; }
       const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(s.nlse2[sb]);
       const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(s.ndelta[sb]);
       const uint64_t c2 = f2_pack(c, c);
       // visible queries of this key row: q >= key - off (causal), key in [klo, kend)
       const int qmin = p.causal ? key - off : -0x7fffffff;
-      const bool need_mask = !key_in || (p.causal && q0 < qmin);
+      const bool need_mask = !key_in || (p.causal && q0 + hf * 64 < qmin);
       if (!mbar_wait_warp(&s.s_full, it & 1, abort_flag, kSiteS)) { ok = false; break; }
       tc_fence_after();
-      uint32_t pk[kTileM / 2];
+      uint32_t pk[32];  // this half's P^T, bf16 pairs
 #pragma unroll
-      for (int cc = 0; cc < kTileM / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t sr[32];
-        tmem_ld32(t_S + lane_off + cc * 32, sr);
+        tmem_ld32(t_S + lane_off + hf * 64 + cc * 32, sr);
         tmem_wait_ld();
         uint32_t pw[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int qa = cc * 32 + 2 * e;
+          const int qa = hf * 64 + cc * 32 + 2 * e;
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), c2,
                            nl2[qa >> 1]),
@@ -356,7 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           pw[e] = pack_bf16x2(p0, p1);
           pk[cc * 16 + e] = pw[e];
         }
-        tmem_st16(t_S + lane_off + cc * 16, pw);
+        // P columns [64 hf + 16 cc, +16) hold scores this warp already loaded
+        tmem_st16(t_S + lane_off + hf * 64 + cc * 16, pw);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -365,15 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dS^T = P^T * (dP^T - D)
       if (!mbar_wait_warp(&s.dp_full, it & 1, abort_flag, kSiteDP)) { ok = false; break; }
       tc_fence_after();
+      const uint32_t blk = ds_base + hf * (kTileN * 128) + row * 128;  // query block hf
 #pragma unroll
-      for (int cc = 0; cc < kTileM / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dr[32];
-        tmem_ld32(t_dP + lane_off + cc * 32, dr);
+        tmem_ld32(t_dP + lane_off + hf * 64 + cc * 32, dr);
         tmem_wait_ld();
         uint32_t dw[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int qa = cc * 32 + 2 * e;
+          const int qa = hf * 64 + cc * 32 + 2 * e;
           const uint64_t dp2 =
               f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
                      nd2[qa >> 1]);
@@ -381,12 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_unpack(f2_mul(bf16x2_to_f2(pk[cc * 16 + e]), dp2), d0, d1);
           dw[e] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(t_dP + lane_off + cc * 16, dw);
-        // shared copy: 32 queries = four 16-byte chunks of query block cc/2
-        const uint32_t blk = ds_base + (cc >> 1) * (kTileN * 128) + row * 128;
+        tmem_st16(t_dP + lane_off + hf * 64 + cc * 16, dw);
+        // shared copy: 32 queries = four 16-byte chunks of query block hf
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          const uint32_t chunk = static_cast<uint32_t>(((cc & 1) * 4 + ch) ^ (row & 7));
+          const uint32_t chunk = static_cast<uint32_t>((cc * 4 + ch) ^ (row & 7));
           st_shared_v4(blk + chunk * 16, dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
         }
       }
@@ -396,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.ds_full);
     }
-    // ---- epilogue: dK = scale * acc, dV = acc  (zeros when no query sees the keys)
+    // ---- epilogue: dK = scale * acc, dV = acc for head-dim columns
+    //      [D/2 hf, D/2 hf + D/2)  (zeros when no query sees the keys)
     if (ok && n_it > 0) ok = mbar_wait_warp(&s.dkv_full, 0, abort_flag, kSiteDKV);
     tc_fence_after();
     // warp-uniform: the TMEM loads below are warp-collective, only the stores
@@ -412,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mul = (pass == 0) ? p.scale : 1.f;
         __nv_bfloat16* dst = (pass == 0) ? dkrow : dvrow;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int c2i = 0; c2i < D / 64; ++c2i) {
+          const int cc = hf * (D / 64) + c2i;  // 32-column chunk of the head dimension
           uint32_t r[32];
           if (n_it > 0) {
             tmem_ld32(src + lane_off + cc * 32, r);
@@ -434,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
-    // ---------------------------------------------- dQ drain (warps 4-7) --
+  } else if (warp < 12) {
+    // --------------------------------------------- dQ drain (warps 8-11) --
     // Each warp moves its 32 query rows of dQ from TMEM into a 128*d-byte slice
     // of this tile's Q/dO stage (32-column boxes, 128-byte swizzle; warps 0-1
     // of the group use the Q buffer, 2-3 the dO buffer) and hands them to TMA
@@ -486,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
