@@ -303,11 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mc = (m == neg_inf()) ? 0.f : m * c;
         // l sums the fp32 weights (it gives the LSE); lr sums the bf16-rounded
         // weights the PV MMA actually multiplies, so O = u / lr is an exactly
-        // normalised combination of the V rows.  Pairs go through the f32x2 pipes.
+        // normalised combination of the V rows.  The fp32 pairs go through the
+        // f32x2 pipes; the rounded weights are added straight from bf16.
         const uint64_t c2 = f2_pack(c, c);
         const uint64_t nmc2 = f2_pack(-mc, -mc);
         uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-        uint64_t sumr2[4] = {0ull, 0ull, 0ull, 0ull};
+        float sr_lo[4] = {0.f, 0.f, 0.f, 0.f}, sr_hi[4] = {0.f, 0.f, 0.f, 0.f};
         // two halves of 64 scores; each half's P (32 packed columns) is stored
         // as soon as it exists, into columns whose S values are already loaded
 #pragma unroll
@@ -324,14 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = ex2_approx(x1);
             pk[jq] = pack_bf16x2(p0, p1);
             sum2[jq & 3] = f2_add(sum2[jq & 3], f2_pack(p0, p1));
-            sumr2[jq & 3] = f2_add(sumr2[jq & 3], bf16x2_to_f2(pk[jq]));
+            add_bf16x2_f32(sr_lo[jq & 3], sr_hi[jq & 3], pk[jq]);
           }
           tmem_st32(t_s + half * 32, pk);
         }
         {
           float a0, a1, b0, b1;
           f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), a0, a1);
-          f2_unpack(f2_add(f2_add(sumr2[0], sumr2[1]), f2_add(sumr2[2], sumr2[3])), b0, b1);
+          b0 = (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]);
+          b1 = (sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]);
           l += a0 + a1;
           lr += b0 + b1;
         }

@@ -398,6 +398,16 @@ __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
   return r;
 }
 
+// acc_lo += low bf16 half of w, acc_hi += high half, each a mixed-precision
+// add (the bf16 operand widens exactly, one fp32 rounding) -- one instruction
+// per half instead of an unpack plus a paired add.
+__device__ __forceinline__ void add_bf16x2_f32(float& acc_lo, float& acc_hi, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(w));
+}
+
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
