@@ -41,7 +41,7 @@ constexpr uint32_t kTmemCols = 512;
 
 // wait-site ids reported in the status word
 enum : unsigned int {
-  kSiteQ = 1, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteVFull, kSitePFull, kSiteSFull,
+  kSiteQ = 1, kSiteKFree, kSiteVFree, kSiteKFull, kSiteVFull, kSitePFull, kSiteSFull,
   kSiteOFull, kSiteDrain
 };
 
@@ -54,7 +54,11 @@ struct FwdSmem {
   __nv_bfloat16 k[NS][NB][kBox];
   __nv_bfloat16 v[NS][NB][kBox];
   uint64_t bar_q;
-  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  uint64_t k_full[NS], v_full[NS];
+  // kv_free[i % NS] completes a phase when every MMA of issue round i has
+  // finished: round i reads K tile i and V tile i - 1, so it frees K stage
+  // i % NS and V stage (i - 1) % NS (one commit per round instead of two).
+  uint64_t kv_free[NS];
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t drain;  // MMA teardown after an abort
   uint32_t tmem_base;
@@ -122,9 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.bar_q, 1);
     for (int i = 0; i < NS; ++i) {
       mbar_init(&s.k_full[i], 1);
-      mbar_init(&s.k_empty[i], 1);
       mbar_init(&s.v_full[i], 1);
-      mbar_init(&s.v_empty[i], 1);
+      mbar_init(&s.kv_free[i], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s.s_full[t], 1);
@@ -162,12 +165,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % NS;
         const int use = j / NS;
         const int c0 = (j0 + j) * kTileN;
-        if (use > 0 && !mbar_wait(&s.k_empty[st], (use - 1) & 1, abort_flag, kSiteKEmpty)) break;
+        // K tile j reuses the stage of K tile j - NS, read in round j - NS
+        if (use > 0 && !mbar_wait(&s.kv_free[st], (use - 1) & 1, abort_flag, kSiteKFree)) break;
         mbar_arrive_expect_tx(&s.k_full[st], NB * kBoxBytes);
         for (int cb = 0; cb < NB; ++cb)
           tma_load_3d_hint(s.k[st][cb], &tk, &s.k_full[st], cb * 64, c0, zkv, keep);
         k_issued = j + 1;
-        if (use > 0 && !mbar_wait(&s.v_empty[st], (use - 1) & 1, abort_flag, kSiteVEmpty)) break;
+        // V tile j reuses the stage of V tile j - NS, read in round j - NS + 1
+        if (use > 0) {
+          const int r = j - NS + 1;
+          if (!mbar_wait(&s.kv_free[r % NS], (r / NS) & 1, abort_flag, kSiteVFree)) break;
+        }
         mbar_arrive_expect_tx(&s.v_full[st], NB * kBoxBytes);
         for (int cb = 0; cb < NB; ++cb)
           tma_load_3d_hint(s.v[st][cb], &tv, &s.v_full[st], cb * 64, c0, zkv, keep);
@@ -198,10 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(&s.bar_q, 0, abort_flag, kSiteQ);
       tc_fence_after();
       for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          if (!mbar_wait(&s.k_full[j % NS], (j / NS) & 1, abort_flag, kSiteKFull)) break;
-          tc_fence_after();
-        }
+        // K and V arrive by TMA: the mbarrier wait alone orders those shared
+        // memory writes before the MMAs (both sides are async-proxy accesses).
+        // Only P, written by other threads' tcgen05.st, needs the tcgen05 fence.
+        if (j < n_tiles && !mbar_wait(&s.k_full[j % NS], (j / NS) & 1, abort_flag, kSiteKFull)) break;
         const uint64_t kd = desc_add(kd0, static_cast<uint32_t>(j % NS) * kStage);
         const uint64_t vd = desc_add(vd0, static_cast<uint32_t>((j + NS - 1) % NS) * kStage);
         for (int t = 0; t < nslots; ++t) {
@@ -235,8 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (j > 0) mma_commit(&s.v_empty[(j - 1) % NS]);
-        if (j < n_tiles) mma_commit(&s.k_empty[j % NS]);
+        if (j < n_tiles) mma_commit(&s.kv_free[j % NS]);
       }
       if (*abort_flag) {
         // every MMA issued so far must finish before TMEM is released
