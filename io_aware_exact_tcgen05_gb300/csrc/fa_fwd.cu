@@ -72,6 +72,52 @@ constexpr size_t fwd_smem_bytes() {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Fast-path bound on a row's fp32 tile sum: every weight stays below 2^64,
+// so P, l and O (at most 2^64 per tile per key block) stay far from fp32
+// overflow while the running max is left as it is.
+constexpr float kFastLimit = 18446744073709551616.0f;  // 2^64
+
+// Scores of keys outside [klo, khi) become -inf (weight 0).
+template <int FIRST, int COUNT>
+__device__ __forceinline__ void mask_scores(uint32_t (&sr)[kTileN], int c0, int klo, int khi) {
+#pragma unroll
+  for (int jj = FIRST; jj < FIRST + COUNT; ++jj) {
+    const int key = c0 + jj;
+    if (key < klo || key >= khi) sr[jj] = 0xff800000u;
+  }
+}
+
+// Weights 2^(s*c - mc) of the 64 scores sr[64*HALF, +64) (nmc2 holds -mc
+// twice), rounded to bf16 pairs and stored to TMEM columns [32*HALF, +32)
+// from t_p.  sum2 gathers the fp32 weights (for l); sr_lo/sr_hi gather the
+// rounded ones the PV MMA multiplies (for lr).
+template <int HALF>
+__device__ __forceinline__ void softmax_half(const uint32_t (&sr)[kTileN], uint64_t c2,
+                                             uint64_t nmc2, uint32_t t_p, uint64_t (&sum2)[4],
+                                             float (&sr_lo)[4], float (&sr_hi)[4]) {
+  uint32_t pk[kTileN / 4];
+#pragma unroll
+  for (int jq = 0; jq < kTileN / 4; ++jq) {
+    const int jj = HALF * (kTileN / 4) + jq;
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * jj]), __uint_as_float(sr[2 * jj + 1])), c2,
+                     nmc2),
+              x0, x1);
+    const float p0 = ex2_approx(x0);
+    const float p1 = ex2_approx(x1);
+    pk[jq] = pack_bf16x2(p0, p1);
+    sum2[jq & 3] = f2_add(sum2[jq & 3], f2_pack(p0, p1));
+    add_bf16x2_f32(sr_lo[jq & 3], sr_hi[jq & 3], pk[jq]);
+  }
+  tmem_st32(t_p + HALF * 32, pk);
+}
+
+__device__ __forceinline__ float sum_f2x4(const uint64_t (&v)[4]) {
+  float a, b;
+  f2_unpack(f2_add(f2_add(v[0], v[1]), f2_add(v[2], v[3])), a, b);
+  return a + b;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -215,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < nslots; ++t) {
           const uint32_t t_s = tmem + t * kTileN;
           if (j > 0) {
-            // O_t += P_t(j-1) V_{j-1}; P_t lives in the first 64 columns of S_t
+            // O_t += P_t(j-1) V_{j-1}; P_t lives in the last 64 columns of S_t
             if (!mbar_wait(&s.p_full[t], (j - 1) & 1, abort_flag, kSitePFull)) { ok = false; break; }
             const int vs = (j - 1) % NS;
             if (t == 0 && !mbar_wait(&s.v_full[vs], ((j - 1) / NS) & 1, abort_flag, kSiteVFull)) {
@@ -224,10 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t t_o = tmem + 2 * kTileN + t * D;
-            mma_ts(t_o, t_s, vd, idesc_pv, j > 1 ? 1u : 0u);
+            const uint32_t t_p = t_s + kTileN / 2;
+            mma_ts(t_o, t_p, vd, idesc_pv, j > 1 ? 1u : 0u);
 #pragma unroll
             for (int kk = 1; kk < kTileN / 16; ++kk)
-              mma_ts(t_o, t_s + kk * 8, desc_add(vd, kk * 16 * 128), idesc_pv, 1u);
+              mma_ts(t_o, t_p + kk * 8, desc_add(vd, kk * 16 * 128), idesc_pv, 1u);
           }
           if (j < n_tiles) {
             // S_t = Q_t K_j^T
@@ -260,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + t * kTileN + lane_off;
     const uint32_t t_o = tmem + 2 * kTileN + t * D + lane_off;
+    const uint32_t t_p = t_s + kTileN / 2;  // P: bf16 pairs in S columns [64, 128)
     const float c = p.scale_log2;
     // keys visible to this row: [klo, khi_row)
     int khi_row = kend;
@@ -279,70 +327,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         const int c0 = (j0 + j) * kTileN;
         const bool need_mask = (c0 < klo) || (c0 + kTileN > khi_row);
-        if (__any_sync(0xffffffffu, need_mask)) {
-#pragma unroll
-          for (int jj = 0; jj < kTileN; ++jj) {
-            const int key = c0 + jj;
-            if (key < klo || key >= khi_row) sr[jj] = 0xff800000u;
-          }
-        }
-        // row max: 8 independent chains of 3-input max
-        float mx8[8];
-#pragma unroll
-        for (int q2 = 0; q2 < 8; ++q2)
-          mx8[q2] = fmaxf(__uint_as_float(sr[q2]), __uint_as_float(sr[q2 + 8]));
-#pragma unroll
-        for (int jj = 16; jj < kTileN; jj += 16)
-#pragma unroll
-          for (int q2 = 0; q2 < 8; ++q2)
-            mx8[q2] = max3f(mx8[q2], __uint_as_float(sr[jj + q2]), __uint_as_float(sr[jj + 8 + q2]));
-        const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
-                               fmaxf(mx8[6], mx8[7]));
-        const float m_new = fmaxf(m, mx);
-        // (m_new - m) is NaN only when both are -inf: no rescale then.
-        const bool grow = (m_new - m) * c > p.rescale_log2;
-        const float alpha = grow ? ex2_approx((m - m_new) * c) : 1.f;  // 0 when m = -inf
-        if (grow) {
-          l *= alpha;
-          lr *= alpha;
-          m = m_new;
-        }
-        const float mc = (m == neg_inf()) ? 0.f : m * c;
-        // l sums the fp32 weights (it gives the LSE); lr sums the bf16-rounded
-        // weights the PV MMA actually multiplies, so O = u / lr is an exactly
-        // normalised combination of the V rows.  The fp32 pairs go through the
-        // f32x2 pipes; the rounded weights are added straight from bf16.
+        const bool masked_tile = __any_sync(0xffffffffu, need_mask);
+        if (masked_tile) mask_scores<0, kTileN>(sr, c0, klo, khi_row);
+        // Fast path: weights relative to the running max as it stands.  The
+        // max only keeps the weights finite, and the fp32 tile sum (needed for
+        // l anyway) bounds every weight of the row, so the tile is checked
+        // after the fact.  A row that has no max yet, or whose tile sum
+        // reaches kFastLimit (or is not finite), sends the warp to the exact
+        // path, which finds the tile max, rescales and recomputes.
+        bool exact = __any_sync(0xffffffffu, m == neg_inf());
         const uint64_t c2 = f2_pack(c, c);
-        const uint64_t nmc2 = f2_pack(-mc, -mc);
         uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
         float sr_lo[4] = {0.f, 0.f, 0.f, 0.f}, sr_hi[4] = {0.f, 0.f, 0.f, 0.f};
-        // two halves of 64 scores; each half's P (32 packed columns) is stored
-        // as soon as it exists, into columns whose S values are already loaded
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[kTileN / 4];
-#pragma unroll
-          for (int jq = 0; jq < kTileN / 4; ++jq) {
-            const int jj = half * (kTileN / 4) + jq;
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * jj]), __uint_as_float(sr[2 * jj + 1])),
-                             c2, nmc2),
-                      x0, x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            pk[jq] = pack_bf16x2(p0, p1);
-            sum2[jq & 3] = f2_add(sum2[jq & 3], f2_pack(p0, p1));
-            add_bf16x2_f32(sr_lo[jq & 3], sr_hi[jq & 3], pk[jq]);
+        if (!exact) {
+          const float mc = m * c;
+          const uint64_t nmc2 = f2_pack(-mc, -mc);
+          softmax_half<0>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi);
+          softmax_half<1>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi);
+          const float ts = sum_f2x4(sum2);
+          exact = __any_sync(0xffffffffu, !(ts < kFastLimit));
+          if (!exact) {
+            l += ts;
+            lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
+                  ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
           }
-          tmem_st32(t_s + half * 32, pk);
         }
-        {
-          float a0, a1, b0, b1;
-          f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), a0, a1);
-          b0 = (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]);
-          b1 = (sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]);
-          l += a0 + a1;
-          lr += b0 + b1;
+        bool grow = false;
+        float alpha = 1.f;
+        if (exact) {
+          // S columns [0, 64) are still in TMEM (P goes to [64, 128)); the
+          // scores of [64, 128) are still in registers.
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+            tmem_ld32(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+          tmem_wait_ld();
+          tmem_wait_st();  // fast-path P stores land before they are rewritten
+          if (masked_tile) mask_scores<0, kTileN / 2>(sr, c0, klo, khi_row);
+          // row max: 8 independent chains of 3-input max
+          float mx8[8];
+#pragma unroll
+          for (int q2 = 0; q2 < 8; ++q2)
+            mx8[q2] = fmaxf(__uint_as_float(sr[q2]), __uint_as_float(sr[q2 + 8]));
+#pragma unroll
+          for (int jj = 16; jj < kTileN; jj += 16)
+#pragma unroll
+            for (int q2 = 0; q2 < 8; ++q2)
+              mx8[q2] = max3f(mx8[q2], __uint_as_float(sr[jj + q2]), __uint_as_float(sr[jj + 8 + q2]));
+          const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                                 fmaxf(mx8[6], mx8[7]));
+          const float m_new = fmaxf(m, mx);
+          // (m_new - m) is NaN only when both are -inf: no rescale then.
+          grow = (m_new - m) * c > p.rescale_log2;
+          alpha = grow ? ex2_approx((m - m_new) * c) : 1.f;  // 0 when m = -inf
+          if (grow) {
+            l *= alpha;
+            lr *= alpha;
+            m = m_new;
+          }
+          const float mc = (m == neg_inf()) ? 0.f : m * c;
+          const uint64_t nmc2 = f2_pack(-mc, -mc);
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2) {
+            sum2[q2] = 0ull;
+            sr_lo[q2] = 0.f;
+            sr_hi[q2] = 0.f;
+          }
+          softmax_half<0>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi);
+          softmax_half<1>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi);
+          l += sum_f2x4(sum2);
+          lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
+                ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
         }
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
           // O_t is quiescent here: PV_t(j-1) completed before S_t(j) was

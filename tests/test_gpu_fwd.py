@@ -85,5 +85,33 @@ def test_large_logits_no_overflow():
     _run(1, 2, 2, 257, 257, 64, False, seed=12, q_mult=30.0)
 
 
+def _run_tensors(q, k, v, causal, scale):
+    o, lse = fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal, scale)
+    torch.cuda.synchronize()
+    ro, rl = orc.fwd(q, k, v, causal, scale)
+    check_o(to_np(o), ro)
+    check_lse(to_np(lse), rl)
+    st, word = fa.fa_device_status()
+    assert st == 0, hex(word)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv,d", [(2, 2, 128), (4, 2, 64)])
+def test_score_jumps_after_first_tile(causal, Hq, Hkv, d):
+    # Later key blocks are scaled by powers of two (exact in bf16) so the
+    # scores of a row jump by hundreds of log2 units well after its first
+    # tile: the weights relative to the running max overflow and the kernel
+    # must redo those tiles from the exact tile max.  The jumps land in both
+    # halves of a tile (keys 200 and 330) and in a ragged last tile; rows
+    # with a zero query see flat scores and never jump.
+    t = workloads.random_qkv(1, Hq, Hkv, 613, 613, d, seed=21, q_mult=4.0)
+    q, k, v = t["q"].float(), t["k"].float(), t["v"]
+    k[:, :, 200:330] *= 8.0
+    k[:, :, 330:600] *= 32.0
+    k[:, :, 600:] *= 64.0
+    q[:, :, 1::5] = 0.0
+    _run_tensors(q.bfloat16(), k.bfloat16(), v, causal, 1.0 / math.sqrt(d))
+
+
 def test_many_tiles_random_scale():
     _run(2, 2, 2, 1100, 1100, 128, True, seed=13, scale=0.05)
