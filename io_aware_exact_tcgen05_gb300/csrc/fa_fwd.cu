@@ -238,43 +238,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------- MMA issuer --
-    if (lane == 0 && n_tiles > 0) {
+    // The whole warp runs this loop (warp-uniform control flow and operands);
+    // one elected lane issues each MMA and commit.
+    if (n_tiles > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, false, true);
       const int nslots = active1 ? 2 : 1;
-      // Descriptors are built once; each MMA only adds a compile-time offset,
-      // so the issuing thread keeps up with the 64-cycle MMAs.
+      // Descriptors are built once; each MMA only adds a compile-time offset.
       constexpr uint32_t kStage = NB * kBoxBytes;  // bytes per K (or V) stage
       const uint64_t qd0 = smem_desc_sw128(smem_u32(s.q[0][0]), 16, 1024);
       const uint64_t qd1 = smem_desc_sw128(smem_u32(s.q[1][0]), 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(smem_u32(s.k[0][0]), 16, 1024);
       const uint64_t vd0 = smem_desc_sw128(smem_u32(s.v[0][0]), NB > 1 ? kBoxBytes : 16u, 1024);
-      bool ok = mbar_wait(&s.bar_q, 0, abort_flag, kSiteQ);
+      bool ok = mbar_wait_warp(&s.bar_q, 0, abort_flag, kSiteQ);
       tc_fence_after();
       for (int j = 0; ok && j <= n_tiles; ++j) {
         // K and V arrive by TMA: the mbarrier wait alone orders those shared
         // memory writes before the MMAs (both sides are async-proxy accesses).
         // Only P, written by other threads' tcgen05.st, needs the tcgen05 fence.
-        if (j < n_tiles && !mbar_wait(&s.k_full[j % NS], (j / NS) & 1, abort_flag, kSiteKFull)) break;
+        if (j < n_tiles && !mbar_wait_warp(&s.k_full[j % NS], (j / NS) & 1, abort_flag, kSiteKFull))
+          break;
         const uint64_t kd = desc_add(kd0, static_cast<uint32_t>(j % NS) * kStage);
         const uint64_t vd = desc_add(vd0, static_cast<uint32_t>((j + NS - 1) % NS) * kStage);
         for (int t = 0; t < nslots; ++t) {
           const uint32_t t_s = tmem + t * kTileN;
           if (j > 0) {
             // O_t += P_t(j-1) V_{j-1}; P_t lives in the last 64 columns of S_t
-            if (!mbar_wait(&s.p_full[t], (j - 1) & 1, abort_flag, kSitePFull)) { ok = false; break; }
+            if (!mbar_wait_warp(&s.p_full[t], (j - 1) & 1, abort_flag, kSitePFull)) {
+              ok = false;
+              break;
+            }
             const int vs = (j - 1) % NS;
-            if (t == 0 && !mbar_wait(&s.v_full[vs], ((j - 1) / NS) & 1, abort_flag, kSiteVFull)) {
+            if (t == 0 && !mbar_wait_warp(&s.v_full[vs], ((j - 1) / NS) & 1, abort_flag, kSiteVFull)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t t_o = tmem + 2 * kTileN + t * D;
             const uint32_t t_p = t_s + kTileN / 2;
-            mma_ts(t_o, t_p, vd, idesc_pv, j > 1 ? 1u : 0u);
+            mma_ts_warp(t_o, t_p, vd, idesc_pv, j > 1 ? 1u : 0u);
 #pragma unroll
             for (int kk = 1; kk < kTileN / 16; ++kk)
-              mma_ts(t_o, t_p + kk * 8, desc_add(vd, kk * 16 * 128), idesc_pv, 1u);
+              mma_ts_warp(t_o, t_p + kk * 8, desc_add(vd, kk * 16 * 128), idesc_pv, 1u);
           }
           if (j < n_tiles) {
             // S_t = Q_t K_j^T
@@ -282,19 +287,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-              mma_ss(t_s, desc_add(qd, off), desc_add(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
+              mma_ss_warp(t_s, desc_add(qd, off), desc_add(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
             }
-            mma_commit(&s.s_full[t]);
+            mma_commit_warp(&s.s_full[t]);
           } else {
-            mma_commit(&s.o_full[t]);
+            mma_commit_warp(&s.o_full[t]);
           }
         }
         if (!ok) break;
-        if (j < n_tiles) mma_commit(&s.kv_free[j % NS]);
+        if (j < n_tiles) mma_commit_warp(&s.kv_free[j % NS]);
       }
-      if (*abort_flag) {
+      if (warp_aborted(abort_flag)) {
         // every MMA issued so far must finish before TMEM is released
-        mma_commit(&s.drain);
+        mma_commit_warp(&s.drain);
         mbar_drain(&s.drain, 0, kSiteDrain);
       }
     }
