@@ -233,7 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------- MMA issuer --
-    if (lane == 0 && n_it > 0) {
+    // The whole warp runs this loop (warp-uniform control flow and operands);
+    // one elected lane issues each MMA and commit.
+    if (n_it > 0) {
       constexpr uint32_t id_kq = idesc_bf16_f32(kTileN, kTileM, false, false);  // S^T, dP^T
       constexpr uint32_t id_acc = idesc_bf16_f32(kTileN, D, false, true);       // dV, dK
       constexpr uint32_t id_dq = idesc_bf16_f32(kTileM, D, true, true);         // dQ
@@ -248,56 +250,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_mn0 = smem_desc_sw128(smem_u32(s.q[0][0]), kLbo, 1024);
       const uint64_t o_mn0 = smem_desc_sw128(smem_u32(s.dout[0][0]), kLbo, 1024);
       const uint64_t ds_mn = smem_desc_sw128(smem_u32(s.ds[0]), kBoxBytes, 1024);
-      bool ok = mbar_wait(&s.kv_full, 0, abort_flag, kSiteKV);
+      bool ok = mbar_wait_warp(&s.kv_full, 0, abort_flag, kSiteKV);
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % kQStages;
         const uint32_t so = static_cast<uint32_t>(st) * kStage;
-        if (!mbar_wait(&s.q_full[st], (it / kQStages) & 1, abort_flag, kSiteQFull)) break;
-        tc_fence_after();
+        // Q and dO arrive by TMA (the mbarrier wait orders them before the
+        // MMAs); the S^T columns this overwrites were last touched by other
+        // threads before p_full of the previous tile, whose fence covers them.
+        if (!mbar_wait_warp(&s.q_full[st], (it / kQStages) & 1, abort_flag, kSiteQFull)) break;
         // S^T = K Q^T  (A = K rows, B = Q rows, both K-major over d)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(t_S, desc_add(k_kmaj, off), desc_add(q_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
+          mma_ss_warp(t_S, desc_add(k_kmaj, off), desc_add(q_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s.s_full);
+        mma_commit_warp(&s.s_full);
         // dP^T = V dO^T; its columns held dQ of the previous tile
-        if (it > 0 && !mbar_wait(&s.dq_empty, (it - 1) & 1, abort_flag, kSiteDQEmpty)) break;
+        if (it > 0 && !mbar_wait_warp(&s.dq_empty, (it - 1) & 1, abort_flag, kSiteDQEmpty)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(t_dP, desc_add(v_kmaj, off), desc_add(o_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
+          mma_ss_warp(t_dP, desc_add(v_kmaj, off), desc_add(o_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s.dp_full);
+        mma_commit_warp(&s.dp_full);
         // dV += P^T dO  (A = P^T in TMEM; B = dO rows, MN-major over d)
-        if (!mbar_wait(&s.p_full, it & 1, abort_flag, kSiteP)) break;
+        if (!mbar_wait_warp(&s.p_full, it & 1, abort_flag, kSiteP)) break;
         tc_fence_after();
-        mma_ts(t_dV, t_S, desc_add(o_mn0, so), id_acc, it > 0 ? 1u : 0u);
+        mma_ts_warp(t_dV, t_S, desc_add(o_mn0, so), id_acc, it > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 1; kk < kTileM / 16; ++kk)
-          mma_ts(t_dV, t_S + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(o_mn0, so + kk * 2048),
+          mma_ts_warp(t_dV, t_S + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(o_mn0, so + kk * 2048),
                  id_acc, 1u);
         // dK += dS^T Q  (A = dS^T in TMEM; B = Q rows, MN-major over d)
-        if (!mbar_wait(&s.ds_full, it & 1, abort_flag, kSiteDS)) break;
+        if (!mbar_wait_warp(&s.ds_full, it & 1, abort_flag, kSiteDS)) break;
         tc_fence_after();
-        mma_ts(t_dK, t_dP, desc_add(q_mn0, so), id_acc, it > 0 ? 1u : 0u);
+        mma_ts_warp(t_dK, t_dP, desc_add(q_mn0, so), id_acc, it > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 1; kk < kTileM / 16; ++kk)
-          mma_ts(t_dK, t_dP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(q_mn0, so + kk * 2048),
+          mma_ts_warp(t_dK, t_dP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(q_mn0, so + kk * 2048),
                  id_acc, 1u);
         // dQ = dS K  (A = dS: shared rows = keys, queries contiguous -> MN-major;
         //             B = K rows, d contiguous -> MN-major), into the dP^T columns
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ss(t_dP, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), id_dq,
+          mma_ss_warp(t_dP, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), id_dq,
                  kk > 0 ? 1u : 0u);
-        mma_commit(&s.dq_full);
-        mma_commit(&s.q_empty[st]);
+        mma_commit_warp(&s.dq_full);
+        mma_commit_warp(&s.q_empty[st]);
       }
-      mma_commit(&s.dkv_full);
-      if (*abort_flag) {
-        mma_commit(&s.drain);
+      mma_commit_warp(&s.dkv_full);
+      if (warp_aborted(abort_flag)) {
+        mma_commit_warp(&s.drain);
         mbar_drain(&s.drain, 0, kSiteDrain);
       }
     }
