@@ -13,6 +13,10 @@
  *                                              the "Flash Attention" history
  *                                              page, 1.1: softmax(QK^T/sqrt d)V)
  *   visible(i, j) <=> k_start[b] <= j < k_end[b]  and  (!causal or j <= i + Sk - Sq)
+ *                     and  key_mask[b][j] != 0 when a key mask is given
+ *                     (per-key boolean mask, FlashAttention_01 page,
+ *                     "interface and implementation constraints": masks and
+ *                     ragged layouts are part of the kernel contract)
  *   m   = max over visible j of s_ij          (mask applied before the max,
  *   l   = sum_vis exp(s_ij - m)                FlashAttention_01 page, "online
  *   u   = sum_vis exp(s_ij - m) v_j            softmax derivation": m, l, u)
@@ -69,10 +73,17 @@ static void load_row(src_t s, long base, long d, double* out) {
   for (long c = 0; c < d; ++c) out[c] = ld(s, base + c);
 }
 
-static int is_visible(long i, long j, long Sq, long Sk, int causal, long ks, long ke) {
+/* km: this batch row's key mask (NULL: every key passes) */
+static int is_visible(long i, long j, long Sq, long Sk, int causal, long ks, long ke,
+                      const unsigned char* km) {
   if (j < ks || j >= ke) return 0;
   if (causal && j > i + Sk - Sq) return 0;
+  if (km && !km[j]) return 0;
   return 1;
+}
+
+static const unsigned char* mask_row(const unsigned char* key_mask, long b, long Sk) {
+  return key_mask ? key_mask + b * Sk : NULL;
 }
 
 static void key_range(const int* k_start, const int* k_end, long b, long Sk, long* ks, long* ke) {
@@ -87,12 +98,13 @@ static void key_range(const int* k_start, const int* k_end, long b, long Sk, lon
  */
 static void row_attention(const double* qrow, src_t k, long kbase, src_t v, long vbase,
                           long n, long d, double scale, long i, long Sq, int causal,
-                          long ks, long ke, double* s, double* m_out, double* l_out,
+                          long ks, long ke, const unsigned char* km, double* s,
+                          double* m_out, double* l_out,
                           double* u, double* o, double* lse_out) {
   double m = -INFINITY;
   long nvis = 0;
   for (long j = 0; j < n; ++j) {
-    if (!is_visible(i, j, Sq, n, causal, ks, ke)) continue;
+    if (!is_visible(i, j, Sq, n, causal, ks, ke, km)) continue;
     double acc = 0.0;
     for (long c = 0; c < d; ++c) acc += qrow[c] * ld(k, kbase + j * d + c);
     s[j] = scale * acc;
@@ -109,7 +121,7 @@ static void row_attention(const double* qrow, src_t k, long kbase, src_t v, long
   }
   double l = 0.0;
   for (long j = 0; j < n; ++j) {
-    if (!is_visible(i, j, Sq, n, causal, ks, ke)) continue;
+    if (!is_visible(i, j, Sq, n, causal, ks, ke, km)) continue;
     double e = exp(s[j] - m);
     l += e;
     for (long c = 0; c < d; ++c) u[c] += e * ld(v, vbase + j * d + c);
@@ -129,7 +141,7 @@ int oracle_row_state(const double* q, const double* k, const double* v, long n, 
   double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
   if (!s) return 1;
   src_t ks = {k, 0}, vs = {v, 0};
-  row_attention(q, ks, 0, vs, 0, n, d, scale, 0, 1, 0, 0, n, s, m, l, u, o, lse);
+  row_attention(q, ks, 0, vs, 0, n, d, scale, 0, 1, 0, 0, n, NULL, s, m, l, u, o, lse);
   free(s);
   return 0;
 }
@@ -138,11 +150,13 @@ int oracle_row_state(const double* q, const double* k, const double* v, long n, 
  * Forward over [B, Hq, Sq, d] queries.  rows == NULL computes every row and
  * writes o[B*Hq*Sq*d], lse[B*Hq*Sq]; otherwise rows holds nrows flat row ids
  * ((b*Hq + h)*Sq + i) and o/lse are packed in that order.  m_out/l_out are
- * optional and follow the same packing.
+ * optional and follow the same packing.  key_mask is NULL or [B, Sk] bytes
+ * (nonzero = the key may be seen).
  */
 int oracle_fwd(const void* q, const void* k, const void* v, int in_bf16, long B, long Hq,
                long Hkv, long Sq, long Sk, long d, int causal, double scale,
-               const int* k_start, const int* k_end, long nrows, const long* rows,
+               const int* k_start, const int* k_end, const unsigned char* key_mask,
+               long nrows, const long* rows,
                double* o, double* lse, double* m_out, double* l_out) {
   if (Hkv <= 0 || Hq % Hkv != 0) return 1;
   const long group = Hq / Hkv;
@@ -170,8 +184,8 @@ int oracle_fwd(const void* q, const void* k, const void* v, int in_bf16, long B,
         load_row(qs, flat * d, d, qrow);
         const long kvbase = (b * Hkv + hk) * Sk * d;
         double m, l;
-        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, s,
-                      &m, &l, u, o + r * d, lse + r);
+        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke,
+                      mask_row(key_mask, b, Sk), s, &m, &l, u, o + r * d, lse + r);
         if (m_out) m_out[r] = m;
         if (l_out) l_out[r] = l;
       }
@@ -189,7 +203,8 @@ int oracle_fwd(const void* q, const void* k, const void* v, int in_bf16, long B,
  */
 int oracle_probs(const void* q, const void* k, const void* v, const void* dout, int in_bf16,
                  long B, long Hq, long Hkv, long Sq, long Sk, long d, int causal,
-                 double scale, const int* k_start, const int* k_end, double* p, double* ds) {
+                 double scale, const int* k_start, const int* k_end,
+                 const unsigned char* key_mask, double* p, double* ds) {
   if (Hkv <= 0 || Hq % Hkv != 0) return 1;
   const long group = Hq / Hkv;
   src_t qs = {q, in_bf16}, kk = {k, in_bf16}, vv = {v, in_bf16}, dos = {dout, in_bf16};
@@ -207,15 +222,16 @@ int oracle_probs(const void* q, const void* k, const void* v, const void* dout, 
         key_range(k_start, k_end, b, Sk, &ks, &ke);
         load_row(qs, flat * d, d, qrow);
         double m, l, lse;
-        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, s, &m,
-                      &l, u, orow, &lse);
+        const unsigned char* km = mask_row(key_mask, b, Sk);
+        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, km, s,
+                      &m, &l, u, orow, &lse);
         double D = 0.0;
         if (ds)
           for (long c = 0; c < d; ++c) D += ld(dos, flat * d + c) * orow[c];
         for (long j = 0; j < Sk; ++j) {
           const long idx = flat * Sk + j;
           double pij = 0.0;
-          if (l > 0.0 && is_visible(i, j, Sq, Sk, causal, ks, ke)) pij = exp(s[j] - m) / l;
+          if (l > 0.0 && is_visible(i, j, Sq, Sk, causal, ks, ke, km)) pij = exp(s[j] - m) / l;
           p[idx] = pij;
           if (ds) {
             double dp = 0.0;
@@ -238,7 +254,8 @@ int oracle_probs(const void* q, const void* k, const void* v, const void* dout, 
  */
 int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, int in_bf16,
                long B, long Hq, long Hkv, long Sq, long Sk, long d, int causal, double scale,
-               const int* k_start, const int* k_end, double* dq, double* dk, double* dv) {
+               const int* k_start, const int* k_end, const unsigned char* key_mask, double* dq,
+               double* dk, double* dv) {
   if (Hkv <= 0 || Hq % Hkv != 0) return 1;
   const long group = Hq / Hkv;
   const long nrow = B * Hq * Sq;
@@ -272,7 +289,8 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
         load_row(qs, flat * d, d, qrow);
         load_row(dos, flat * d, d, dorow);
         double lse;
-        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, s,
+        const unsigned char* km = mask_row(key_mask, b, Sk);
+        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, km, s,
                       &M[flat], &L[flat], u, orow, &lse);
         double D = 0.0;
         for (long c = 0; c < d; ++c) D += dorow[c] * orow[c];
@@ -281,7 +299,7 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
         for (long c = 0; c < d; ++c) dqr[c] = 0.0;
         if (L[flat] <= 0.0) continue;
         for (long j = 0; j < Sk; ++j) {
-          if (!is_visible(i, j, Sq, Sk, causal, ks, ke)) continue;
+          if (!is_visible(i, j, Sq, Sk, causal, ks, ke, km)) continue;
           const double pij = exp(s[j] - M[flat]) / L[flat];
           double dp = 0.0;
           for (long c = 0; c < d; ++c) dp += dorow[c] * ld(vv, kvbase + j * d + c);
@@ -315,6 +333,7 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
         const long b = flatk / (Sk * Hkv);
         long ks, ke;
         key_range(k_start, k_end, b, Sk, &ks, &ke);
+        const unsigned char* km = mask_row(key_mask, b, Sk);
         load_row(kk, flatk * d, d, krow);
         load_row(vv, flatk * d, d, vrow);
         double* dkr = dk + flatk * d;
@@ -323,7 +342,7 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
         for (long g = 0; g < group; ++g) {
           const long h = hk * group + g;
           for (long i = 0; i < Sq; ++i) {
-            if (!is_visible(i, j, Sq, Sk, causal, ks, ke)) continue;
+            if (!is_visible(i, j, Sq, Sk, causal, ks, ke, km)) continue;
             const long flat = (b * Hq + h) * Sq + i;
             if (L[flat] <= 0.0) continue;
             double sij = 0.0, dp = 0.0;

@@ -49,11 +49,11 @@ def _load():
             P = ctypes.c_void_p
             L = ctypes.c_long
             lib.oracle_fwd.argtypes = [P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
-                                       ctypes.c_double, P, P, L, P, P, P, P, P]
+                                       ctypes.c_double, P, P, P, L, P, P, P, P, P]
             lib.oracle_bwd.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
-                                       ctypes.c_double, P, P, P, P, P]
+                                       ctypes.c_double, P, P, P, P, P, P]
             lib.oracle_probs.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
-                                         ctypes.c_double, P, P, P, P]
+                                         ctypes.c_double, P, P, P, P, P]
             lib.oracle_row_state.argtypes = [P, P, P, L, L, ctypes.c_double, P, P, P, P, P]
             for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_probs, lib.oracle_row_state):
                 f.restype = ctypes.c_int
@@ -98,18 +98,37 @@ def _i32(x, B):
     return a
 
 
+def _mask(x, B, Sk):
+    """Key mask as contiguous uint8 [B, Sk] (nonzero = the key may be seen)."""
+    if x is None:
+        return None
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(np.asarray(x) != 0, dtype=np.uint8)
+    if a.ndim == 1 and B == 1:
+        a = a[None]
+    assert a.shape == (B, Sk), a.shape
+    return a
+
+
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
 
 
 def fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, rows=None,
-        return_stats: bool = False):
+        return_stats: bool = False, key_mask=None):
     """Forward O and LSE from the definition (the "Flash Attention" history page
     1.1-1.2; FlashAttention_01 page, online-softmax derivation, masking rule).
 
     q: [B,Hq,Sq,d], k/v: [B,Hkv,Sk,d] (bf16 torch tensors or float arrays).
     rows: optional flat row ids ((b*Hq+h)*Sq+i); results are then packed
     [len(rows), d] / [len(rows)].  Fully masked rows give O=0, LSE=-inf.
+    key_mask: optional [B, Sk] booleans; a key whose entry is false is not
+    visible to any query of that batch row.
     """
     qa, bf = _as_input(q)
     ka, bk = _as_input(k)
@@ -130,8 +149,8 @@ def fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, rows=None
     m = np.empty((n,), np.float64) if return_stats else None
     l = np.empty((n,), np.float64) if return_stats else None
     rc = _load().oracle_fwd(_ptr(qa), _ptr(ka), _ptr(va), bf, B, Hq, Hkv, Sq, Sk, d, int(causal),
-                            float(scale), _ptr(ks), _ptr(ke), n, _ptr(rr), _ptr(o), _ptr(lse),
-                            _ptr(m), _ptr(l))
+                            float(scale), _ptr(ks), _ptr(ke), _ptr(_mask(key_mask, B, Sk)), n,
+                            _ptr(rr), _ptr(o), _ptr(lse), _ptr(m), _ptr(l))
     if rc:
         raise RuntimeError(f"oracle_fwd failed ({rc})")
     if rows is None:
@@ -145,7 +164,7 @@ def fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, rows=None
     return o, lse
 
 
-def bwd(q, k, v, dout, causal: bool, scale: float, k_start=None, k_end=None):
+def bwd(q, k, v, dout, causal: bool, scale: float, k_start=None, k_end=None, key_mask=None):
     """dQ, dK, dV from the definition (FlashAttention_01 page, "why the backward
     can recompute" and the chain-rule section): dV=P^T dO, dP=dO V^T,
     dS=P*(dP-rowsum(dO*O)), dQ=scale dS K, dK=scale dS^T Q; GQA heads summed."""
@@ -160,13 +179,15 @@ def bwd(q, k, v, dout, causal: bool, scale: float, k_start=None, k_end=None):
     dv = np.empty((B, Hkv, Sk, d), np.float64)
     rc = _load().oracle_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), bf, B, Hq, Hkv, Sq, Sk, d,
                             int(causal), float(scale), _ptr(_i32(k_start, B)),
-                            _ptr(_i32(k_end, B)), _ptr(dq), _ptr(dk), _ptr(dv))
+                            _ptr(_i32(k_end, B)), _ptr(_mask(key_mask, B, Sk)), _ptr(dq),
+                            _ptr(dk), _ptr(dv))
     if rc:
         raise RuntimeError(f"oracle_bwd failed ({rc})")
     return dq, dk, dv
 
 
-def probs(q, k, v, causal: bool, scale: float, dout=None, k_start=None, k_end=None):
+def probs(q, k, v, causal: bool, scale: float, dout=None, k_start=None, k_end=None,
+          key_mask=None):
     """Dense P [B,Hq,Sq,Sk] and, when dout is given, dS (small problems only)."""
     qa, bf = _as_input(q)
     ka, _ = _as_input(k)
@@ -178,7 +199,8 @@ def probs(q, k, v, causal: bool, scale: float, dout=None, k_start=None, k_end=No
     ds = np.empty((B, Hq, Sq, Sk), np.float64) if dout is not None else None
     rc = _load().oracle_probs(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), bf, B, Hq, Hkv, Sq, Sk, d,
                               int(causal), float(scale), _ptr(_i32(k_start, B)),
-                              _ptr(_i32(k_end, B)), _ptr(p), _ptr(ds))
+                              _ptr(_i32(k_end, B)), _ptr(_mask(key_mask, B, Sk)), _ptr(p),
+                              _ptr(ds))
     if rc:
         raise RuntimeError(f"oracle_probs failed ({rc})")
     return (p, ds) if dout is not None else p
@@ -209,3 +231,69 @@ def decode(q, k_cache, v_cache, seqlens_k, scale: float, rows=None):
     B = q.shape[0]
     return fwd(q, k_cache, v_cache, causal=False, scale=scale, k_start=None,
                k_end=_i32(seqlens_k, B), rows=rows)
+
+
+def _seq_bounds(cu):
+    try:
+        import torch
+        if isinstance(cu, torch.Tensor):
+            cu = cu.cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    cu = np.asarray(cu, dtype=np.int64)
+    return [(int(cu[i]), int(cu[i + 1])) for i in range(len(cu) - 1)]
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: float, key_mask=None):
+    """Packed ragged forward: q [Hq, total_q, d], k/v [Hkv, total_k, d]; sequence
+    s owns packed query rows [cu_q[s], cu_q[s+1]) and keys [cu_k[s], cu_k[s+1])
+    and is attended on its own (FlashAttention_01 page, "interface and
+    implementation constraints": logical rows of a ragged layout are told apart
+    from packed rows).  Causal alignment is bottom-right within each sequence.
+    key_mask: optional [total_k] booleans over packed keys.  Returns O
+    [Hq, total_q, d] and LSE [Hq, total_q]; each sequence is the plain forward
+    on its own rows and keys."""
+    qa, bf = _as_input(q)
+    ka, _ = _as_input(k)
+    va, _ = _as_input(v)
+    Hq, total_q, d = qa.shape
+    km = None if key_mask is None else _mask(key_mask, 1, ka.shape[1])[0]
+    o = np.zeros((Hq, total_q, d), np.float64)
+    lse = np.full((Hq, total_q), -np.inf)
+    for (q0, q1), (k0, k1) in zip(_seq_bounds(cu_seqlens_q), _seq_bounds(cu_seqlens_k)):
+        if q1 <= q0:
+            continue
+        if k1 <= k0:  # no keys: every row is fully masked
+            continue
+        mk = None if km is None else km[None, k0:k1]
+        os_, ls_ = fwd(qa[None, :, q0:q1], ka[None, :, k0:k1], va[None, :, k0:k1], causal, scale,
+                       key_mask=mk)
+        o[:, q0:q1] = os_[0]
+        lse[:, q0:q1] = ls_[0]
+    return o, lse
+
+
+def bwd_varlen(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: float,
+               key_mask=None):
+    """Packed ragged backward, each sequence on its own (see fwd_varlen):
+    dQ [Hq, total_q, d], dK/dV [Hkv, total_k, d]."""
+    qa, bf = _as_input(q)
+    ka, _ = _as_input(k)
+    va, _ = _as_input(v)
+    da, _ = _as_input(dout)
+    Hq, total_q, d = qa.shape
+    Hkv, total_k, _ = ka.shape
+    km = None if key_mask is None else _mask(key_mask, 1, total_k)[0]
+    dq = np.zeros((Hq, total_q, d), np.float64)
+    dk = np.zeros((Hkv, total_k, d), np.float64)
+    dv = np.zeros((Hkv, total_k, d), np.float64)
+    for (q0, q1), (k0, k1) in zip(_seq_bounds(cu_seqlens_q), _seq_bounds(cu_seqlens_k)):
+        if q1 <= q0 or k1 <= k0:
+            continue
+        mk = None if km is None else km[None, k0:k1]
+        a, b_, c = bwd(qa[None, :, q0:q1], ka[None, :, k0:k1], va[None, :, k0:k1],
+                       da[None, :, q0:q1], causal, scale, key_mask=mk)
+        dq[:, q0:q1] = a[0]
+        dk[:, k0:k1] = b_[0]
+        dv[:, k0:k1] = c[0]
+    return dq, dk, dv

@@ -189,6 +189,145 @@ def test_backward_matches_torch_autograd_fp64(case):
     assert np.all(dq[~live.numpy()] == 0.0)
 
 
+# --- per-key boolean masks and packed ragged sequences (FlashAttention_01
+#     page, "interface and implementation constraints": masks and ragged
+#     layouts are part of the kernel contract; logical vs packed rows) ---
+
+def _key_mask(B, Sk, seed, drop=0.3):
+    g = torch.Generator().manual_seed(seed)
+    return torch.rand(B, Sk, generator=g) >= drop
+
+
+def _sdpa_ref(q, k, v, mask, scale, do=None):
+    """fp64 torch SDPA with a boolean [B,1,Sq,Sk] mask: (O, LSE, live rows) and,
+    with do, the autograd gradients (dead rows get zero upstream grad)."""
+    B, Hq, Sq, _ = q.shape
+    Hkv = k.shape[1]
+    live = mask.any(-1).expand(B, Hq, Sq)
+    qt, kt, vt = (x.clone().requires_grad_() for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt, vt, attn_mask=mask, scale=scale, enable_gqa=(Hq != Hkv))
+    ref = torch.where(live[..., None], ref, torch.zeros_like(ref))
+    s = torch.einsum("bhid,bhjd->bhij", q, k.repeat_interleave(Hq // Hkv, 1)) * scale
+    lse = torch.logsumexp(s.masked_fill(~mask, -math.inf), -1)
+    grads = None
+    if do is not None:
+        ref.backward(do.masked_fill(~live[..., None], 0.0))
+        grads = (qt.grad, kt.grad, vt.grad)
+    return ref.detach(), lse, live, grads
+
+
+MASK_CASES = [
+    # B, Hq, Hkv, Sq, Sk, d, causal
+    (2, 4, 2, 29, 37, 16, True),
+    (1, 2, 2, 40, 40, 8, False),
+    (2, 2, 1, 17, 23, 16, True),
+]
+
+
+@pytest.mark.parametrize("case", MASK_CASES)
+def test_key_mask_matches_torch_sdpa_fp64(case):
+    B, Hq, Hkv, Sq, Sk, d, causal = case
+    q = _rand((B, Hq, Sq, d), 40)
+    k = _rand((B, Hkv, Sk, d), 41)
+    v = _rand((B, Hkv, Sk, d), 42)
+    do = _rand((B, Hq, Sq, d), 43)
+    km = _key_mask(B, Sk, 44)
+    km[0, :Sk // 2] = False  # long masked run: some causal rows see nothing
+    scale = 1.0 / math.sqrt(d)
+    mask = _mask(Sq, Sk, causal, [0] * B, [Sk] * B, B) & km[:, None, None, :]
+    ref, ref_lse, live, (gq, gk, gv) = _sdpa_ref(q, k, v, mask, scale, do)
+    o, lse = orc.fwd(q, k, v, causal, scale, key_mask=km)
+    L = live.numpy()
+    assert L.any() and (L.all() != causal)  # causal rows 0.. see only masked keys
+    assert np.abs(o[L] - ref[live].numpy()).max() < 1e-12
+    assert np.abs(lse[L] - ref_lse[live].numpy()).max() < 1e-12
+    assert np.all(o[~L] == 0.0) and np.all(lse[~L] == -np.inf)
+    dq, dk, dv = orc.bwd(q, k, v, do, causal, scale, key_mask=km)
+    for mine, theirs in ((dq, gq), (dk, gk), (dv, gv)):
+        assert np.abs(mine - theirs.numpy()).max() < 1e-11
+    # a masked key gets exactly zero gradient and zero probability
+    dead_keys = ~km.numpy()
+    for b in range(B):
+        assert np.all(dk[b][:, dead_keys[b]] == 0.0) and np.all(dv[b][:, dead_keys[b]] == 0.0)
+    p = orc.probs(q, k, v, causal, scale, key_mask=km)
+    assert np.all(p[..., :][np.broadcast_to(dead_keys[:, None, None, :], p.shape)] == 0.0)
+
+
+def test_interval_key_mask_equals_key_interval():
+    B, Hq, Hkv, Sq, Sk, d = 2, 2, 1, 21, 30, 8
+    q = _rand((B, Hq, Sq, d), 50)
+    k = _rand((B, Hkv, Sk, d), 51)
+    v = _rand((B, Hkv, Sk, d), 52)
+    do = _rand((B, Hq, Sq, d), 53)
+    ks, ke = [4, 0], [30, 17]
+    j = torch.arange(Sk)[None, :]
+    km = (j >= torch.tensor(ks)[:, None]) & (j < torch.tensor(ke)[:, None])
+    for causal in (False, True):
+        a = orc.fwd(q, k, v, causal, 0.3, k_start=ks, k_end=ke)
+        b = orc.fwd(q, k, v, causal, 0.3, key_mask=km)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
+        ga = orc.bwd(q, k, v, do, causal, 0.3, k_start=ks, k_end=ke)
+        gb = orc.bwd(q, k, v, do, causal, 0.3, key_mask=km)
+        assert all(np.array_equal(x, y) for x, y in zip(ga, gb))
+
+
+VARLEN_Q = [5, 0, 17, 33, 3]
+VARLEN_K = [9, 4, 17, 20, 0]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_matches_per_sequence_torch_sdpa(causal):
+    Hq, Hkv, d = 4, 2, 16
+    cu_q = np.concatenate([[0], np.cumsum(VARLEN_Q)])
+    cu_k = np.concatenate([[0], np.cumsum(VARLEN_K)])
+    q = _rand((Hq, int(cu_q[-1]), d), 60)
+    k = _rand((Hkv, int(cu_k[-1]), d), 61)
+    v = _rand((Hkv, int(cu_k[-1]), d), 62)
+    do = _rand((Hq, int(cu_q[-1]), d), 63)
+    km = _key_mask(1, int(cu_k[-1]), 64, drop=0.2)[0]
+    scale = 1.0 / math.sqrt(d)
+    for use_mask in (False, True):
+        kmask = km if use_mask else None
+        o, lse = orc.fwd_varlen(q, k, v, cu_q, cu_k, causal, scale, key_mask=kmask)
+        dq, dk, dv = orc.bwd_varlen(q, k, v, do, cu_q, cu_k, causal, scale, key_mask=kmask)
+        for s in range(len(VARLEN_Q)):
+            q0, q1, k0, k1 = int(cu_q[s]), int(cu_q[s + 1]), int(cu_k[s]), int(cu_k[s + 1])
+            if q1 == q0:
+                continue
+            if k1 == k0:  # a sequence without keys: its rows are fully masked
+                assert np.all(o[:, q0:q1] == 0.0) and np.all(lse[:, q0:q1] == -np.inf)
+                assert np.all(dq[:, q0:q1] == 0.0)
+                continue
+            Sq, Sk = q1 - q0, k1 - k0
+            mask = _mask(Sq, Sk, causal, [0], [Sk], 1)
+            if use_mask:
+                mask = mask & km[None, None, None, k0:k1]
+            ref, ref_lse, live, (gq, gk, gv) = _sdpa_ref(
+                q[None, :, q0:q1], k[None, :, k0:k1], v[None, :, k0:k1], mask, scale,
+                do[None, :, q0:q1])
+            L = live[0].numpy()
+            assert np.abs(o[:, q0:q1][L] - ref[0][live[0]].numpy()).max() < 1e-12
+            assert np.abs(lse[:, q0:q1][L] - ref_lse[0][live[0]].numpy()).max() < 1e-12
+            assert np.all(lse[:, q0:q1][~L] == -np.inf)
+            assert np.abs(dq[:, q0:q1] - gq[0].numpy()).max() < 1e-11
+            assert np.abs(dk[:, k0:k1] - gk[0].numpy()).max() < 1e-11
+            assert np.abs(dv[:, k0:k1] - gv[0].numpy()).max() < 1e-11
+
+
+def test_varlen_equal_lengths_equals_batched():
+    B, Hq, Hkv, S, d = 3, 2, 1, 12, 8
+    q = _rand((B, Hq, S, d), 70)
+    k = _rand((B, Hkv, S, d), 71)
+    v = _rand((B, Hkv, S, d), 72)
+    pack = lambda x: x.permute(1, 0, 2, 3).reshape(x.shape[1], B * S, d)  # noqa: E731
+    cu = np.arange(B + 1) * S
+    o, lse = orc.fwd_varlen(pack(q), pack(k), pack(v), cu, cu, True, 0.4)
+    ob, lb = orc.fwd(q, k, v, True, 0.4)
+    assert np.array_equal(o, ob.transpose(1, 0, 2, 3).reshape(Hq, B * S, d))
+    assert np.array_equal(lse, lb.transpose(1, 0, 2).reshape(Hq, B * S))
+
+
 # --- chain-rule section: central differences on the 2x3x2 masked example ---
 
 def _loss(q, k, v):
