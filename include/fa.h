@@ -100,6 +100,74 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const int32_t* k_end, void* workspace, size_t workspace_bytes,
                  cudaStream_t stream);
 
+/*
+ * Per-key boolean masks and packed ragged ("varlen") sequences.
+ * Follows: FlashAttention_01 page, "interface and implementation constraints"
+ * (masks and ragged layouts are part of the kernel contract; statistics cover
+ * only valid rows; a ragged layout tells logical row numbers from packed ones).
+ *
+ * Key mask bits: key j of mask row r is visible iff bit (j % 32) of word
+ * bits[r * fa_key_mask_words(Sk) + j / 32] is set.  A hidden key is treated
+ * like a key outside [k_start, k_end): it gets weight 0 in the softmax and
+ * zero dK/dV.  A row that sees no key gives O = 0, LSE = -inf.  The bits
+ * buffer is caller-owned device memory, 16-byte aligned; bits past Sk are
+ * ignored.  fa_pack_key_mask builds it from one byte per key.
+ */
+size_t fa_key_mask_words(int Sk); /* uint32 words per mask row: 4 * ceil(Sk / 128) */
+
+/* bits[rows][fa_key_mask_words(Sk)] = packed (mask[rows][Sk] != 0); device
+   buffers, asynchronous on stream.  mask needs no alignment. */
+fa_status fa_pack_key_mask(const uint8_t* mask, uint32_t* bits, int rows, int Sk,
+                           cudaStream_t stream);
+
+/* fa_fwd with a per-(batch row, key) mask: key_mask_bits has B mask rows
+   (NULL = no mask, exactly fa_fwd). */
+fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                        const int32_t* k_start, const int32_t* k_end,
+                        const uint32_t* key_mask_bits, cudaStream_t stream);
+
+/* fa_bwd with the same key mask the forward used (NULL = exactly fa_bwd). */
+fa_status fa_bwd_masked(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                        const int32_t* k_start, const int32_t* k_end,
+                        const uint32_t* key_mask_bits, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+/*
+ * Packed ragged forward.  nseq sequences are concatenated along the row
+ * axis: q/o [Hq, total_q, d], k/v [Hkv, total_k, d], lse [Hq, total_q].
+ * Sequence s owns packed query rows [cu_seqlens_q[s], cu_seqlens_q[s+1]) and
+ * packed keys [cu_seqlens_k[s], cu_seqlens_k[s+1]) and attends only within
+ * itself; the causal rule is bottom-right within the sequence (logical key
+ * j' <= logical row i' + Sk_s - Sq_s).  cu_seqlens_* are device int32[nseq+1],
+ * non-decreasing, from 0 to total_q / total_k (values are clamped to
+ * [0, total]).  max_seqlen_q/k are host upper bounds on the sequences'
+ * query and key counts; they size the grid, and rows or keys of a sequence
+ * past them are not processed (their outputs are left unwritten).  Packed
+ * rows or keys that belong to no sequence are not written either.
+ * Rows of a sequence without keys get O = 0 and LSE = -inf.  key_mask_bits
+ * (nullable) is one mask row over the packed keys.
+ */
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                        int Hkv, int d, int causal, float scale, const uint32_t* key_mask_bits,
+                        cudaStream_t stream);
+
+/*
+ * Packed ragged backward, the layout and arguments of fa_fwd_varlen: dq
+ * [Hq, total_q, d] and dk/dv [Hkv, total_k, d] are written; workspace holds
+ * fa_bwd_workspace_size(1, Hq, total_q, d) bytes.
+ */
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                        int Hkv, int d, int causal, float scale, const uint32_t* key_mask_bits,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Bytes of device workspace fa_decode needs for a cache of Sk_max positions:
    per (b, query head, split) partial outputs and logsumexps. */
 size_t fa_decode_workspace_size(int B, int Hq, int Sk_max, int d);

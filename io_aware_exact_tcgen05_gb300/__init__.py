@@ -25,9 +25,9 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_decode", "fa_decode_workspace_size",
-            "fa_decode_noalloc", "fa_device_status", "fa_profile_next_launch",
-            "fa_status_string",
-            "fa_last_error_detail", "fa_version")
+            "fa_decode_noalloc", "fa_fwd_masked", "fa_bwd_masked", "fa_fwd_varlen",
+            "fa_bwd_varlen", "fa_key_mask_words", "fa_pack_key_mask", "fa_device_status",
+            "fa_profile_next_launch", "fa_status_string", "fa_last_error_detail", "fa_version")
 
 _lib = None
 
@@ -51,6 +51,18 @@ def load_library(path: str = LIB_PATH):
     lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, Z, P]
     lib.fa_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P, Z, P]
     lib.fa_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
+    lib.fa_fwd_masked.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P]
+    lib.fa_bwd_masked.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P, Z,
+                                  P]
+    lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P]
+    lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P,
+                                  P, Z, P]
+    lib.fa_key_mask_words.argtypes = [I]
+    lib.fa_key_mask_words.restype = Z
+    lib.fa_pack_key_mask.argtypes = [P, P, I, I, P]
+    for f in (lib.fa_fwd_masked, lib.fa_bwd_masked, lib.fa_fwd_varlen, lib.fa_bwd_varlen,
+              lib.fa_pack_key_mask):
+        f.restype = I
     lib.fa_decode_noalloc.restype = I
     lib.fa_bwd_workspace_size.argtypes = [I, I, I, I]
     lib.fa_bwd_workspace_size.restype = Z
@@ -95,11 +107,46 @@ def _need(t, name, dtype, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims")
 
 
+def fa_key_mask_words(Sk: int) -> int:
+    return int(load_library().fa_key_mask_words(Sk))
+
+
+def fa_pack_key_mask(mask, stream=None):
+    """Visibility bit words [rows, fa_key_mask_words(Sk)] (int32 storage of the
+    uint32 words) from a bool/uint8 CUDA mask [rows, Sk], via fa_pack_key_mask."""
+    lib = load_library()
+    if not isinstance(mask, torch.Tensor) or not mask.is_cuda:
+        raise TypeError("mask must be a CUDA tensor")
+    if mask.dtype not in (torch.bool, torch.uint8) or not mask.is_contiguous() or mask.dim() != 2:
+        raise ValueError("mask must be a contiguous 2-D bool or uint8 tensor")
+    rows, Sk = mask.shape
+    bits = torch.empty(rows, fa_key_mask_words(Sk), dtype=torch.int32, device=mask.device)
+    _check(lib.fa_pack_key_mask(_ptr(mask), _ptr(bits), rows, Sk, _stream(stream)),
+           "fa_pack_key_mask")
+    return bits
+
+
+def _mask_bits(key_mask, rows, Sk, stream):
+    """Bit words for a key mask given as bools [rows, Sk] (packed on the
+    device) or as bit words already; None when there is no mask."""
+    if key_mask is None:
+        return None
+    if key_mask.dtype in (torch.bool, torch.uint8):
+        if tuple(key_mask.shape) != (rows, Sk):
+            raise ValueError(f"key_mask must be [{rows}, {Sk}], got {tuple(key_mask.shape)}")
+        return fa_pack_key_mask(key_mask.contiguous(), stream)
+    _need(key_mask, "key_mask bits", torch.int32, 2)
+    if tuple(key_mask.shape) != (rows, fa_key_mask_words(Sk)):
+        raise ValueError("key_mask bit words have the wrong shape")
+    return key_mask
+
+
 def fa_fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, o=None, lse=None,
-           stream=None):
+           stream=None, key_mask=None):
     """O, LSE = attention(q, k, v) via the library's fa_fwd (see include/fa.h).
     q [B,Hq,Sq,d], k/v [B,Hkv,Sk,d] bf16 CUDA tensors; k_start/k_end optional
-    int32 [B] CUDA tensors.  Returns (o, lse)."""
+    int32 [B] CUDA tensors; key_mask optional [B, Sk] bool CUDA tensor (or its
+    fa_pack_key_mask words), giving fa_fwd_masked.  Returns (o, lse)."""
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, 4)
@@ -112,9 +159,17 @@ def fa_fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, o=None
     for t, n in ((k_start, "k_start"), (k_end, "k_end")):
         if t is not None:
             _need(t, n, torch.int32, 1)
-    st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
-                    int(bool(causal)), float(scale), _ptr(k_start), _ptr(k_end), _stream(stream))
-    _check(st, "fa_fwd")
+    bits = _mask_bits(key_mask, B, Sk, stream)
+    if bits is None:
+        st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
+                        int(bool(causal)), float(scale), _ptr(k_start), _ptr(k_end),
+                        _stream(stream))
+        _check(st, "fa_fwd")
+    else:
+        st = lib.fa_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk,
+                               d, int(bool(causal)), float(scale), _ptr(k_start), _ptr(k_end),
+                               _ptr(bits), _stream(stream))
+        _check(st, "fa_fwd_masked")
     return o, lse
 
 
@@ -123,8 +178,9 @@ def fa_bwd_workspace_size(B, Hq, Sq, d) -> int:
 
 
 def fa_bwd(q, k, v, o, dout, lse, causal: bool, scale: float, k_start=None, k_end=None,
-           dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dQ, dK, dV by recomputation via the library's fa_bwd.  Returns (dq, dk, dv)."""
+           dq=None, dk=None, dv=None, workspace=None, stream=None, key_mask=None):
+    """dQ, dK, dV by recomputation via the library's fa_bwd (fa_bwd_masked
+    when key_mask is given; it must be the forward's).  Returns (dq, dk, dv)."""
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _need(t, n, torch.bfloat16, 4)
@@ -137,11 +193,77 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool, scale: float, k_start=None, k_en
     nbytes = fa_bwd_workspace_size(B, Hq, Sq, d)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
-                    _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d, int(bool(causal)), float(scale),
-                    _ptr(k_start), _ptr(k_end), _ptr(workspace), workspace.numel(),
-                    _stream(stream))
-    _check(st, "fa_bwd")
+    bits = _mask_bits(key_mask, B, Sk, stream)
+    if bits is None:
+        st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                        _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d, int(bool(causal)),
+                        float(scale), _ptr(k_start), _ptr(k_end), _ptr(workspace),
+                        workspace.numel(), _stream(stream))
+        _check(st, "fa_bwd")
+    else:
+        st = lib.fa_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d,
+                               int(bool(causal)), float(scale), _ptr(k_start), _ptr(k_end),
+                               _ptr(bits), _ptr(workspace), workspace.numel(), _stream(stream))
+        _check(st, "fa_bwd_masked")
+    return dq, dk, dv
+
+
+def _varlen_args(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k):
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        _need(t, n, torch.int32, 1)
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold nseq + 1 >= 2 offsets")
+    Hq, total_q, d = q.shape
+    Hkv, total_k, _ = k.shape
+    return cu_seqlens_q.numel() - 1, Hq, Hkv, total_q, total_k, d
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                  causal: bool, scale: float, key_mask=None, o=None, lse=None, stream=None):
+    """Packed ragged forward via fa_fwd_varlen: q [Hq,total_q,d], k/v
+    [Hkv,total_k,d] bf16; cu_seqlens_* int32 [nseq+1] CUDA offsets; key_mask
+    optional [total_k] bools over the packed keys.  Returns (o, lse [Hq,total_q])."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 3)
+    nseq, Hq, Hkv, total_q, total_k, d = _varlen_args(q, k, cu_seqlens_q, cu_seqlens_k,
+                                                      max_seqlen_q, max_seqlen_k)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(Hq, total_q, dtype=torch.float32, device=q.device) if lse is None else lse
+    bits = _mask_bits(None if key_mask is None else key_mask.reshape(1, -1), 1, total_k, stream)
+    st = lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                           _ptr(cu_seqlens_k), nseq, int(max_seqlen_q), int(max_seqlen_k),
+                           total_q, total_k, Hq, Hkv, d, int(bool(causal)), float(scale),
+                           _ptr(bits), _stream(stream))
+    _check(st, "fa_fwd_varlen")
+    return o, lse
+
+
+def fa_bwd_varlen(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, causal: bool, scale: float, key_mask=None, dq=None,
+                  dk=None, dv=None, workspace=None, stream=None):
+    """Packed ragged backward via fa_bwd_varlen (layout of fa_fwd_varlen).
+    Returns (dq [Hq,total_q,d], dk, dv [Hkv,total_k,d])."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _need(t, n, torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    nseq, Hq, Hkv, total_q, total_k, d = _varlen_args(q, k, cu_seqlens_q, cu_seqlens_k,
+                                                      max_seqlen_q, max_seqlen_k)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_size(1, Hq, total_q, d), dtype=torch.uint8,
+                                device=q.device)
+    bits = _mask_bits(None if key_mask is None else key_mask.reshape(1, -1), 1, total_k, stream)
+    st = lib.fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                           _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), nseq,
+                           int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, Hq, Hkv, d,
+                           int(bool(causal)), float(scale), _ptr(bits), _ptr(workspace),
+                           workspace.numel(), _stream(stream))
+    _check(st, "fa_bwd_varlen")
     return dq, dk, dv
 
 

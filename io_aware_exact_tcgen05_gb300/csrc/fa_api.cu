@@ -156,21 +156,51 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
     if (_s != FA_OK) return _s;      \
   } while (0)
 
-}  // namespace
+// Where a launch's rows and keys come from: the batched layout (grid batch
+// = B, optional per-batch key interval) or packed ragged sequences.
+struct SeqLayout {
+  int grid_b;          // B, or the sequence count
+  int longest_q;       // rows of the longest unit (Sq, or max_seqlen_q)
+  int longest_k;       // keys of the longest unit (Sk, or max_seqlen_k)
+  const int32_t* k_start;
+  const int32_t* k_end;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+};
 
-extern "C" {
+fa_status varlen_layout(const int32_t* cu_q, const int32_t* cu_k, int nseq, int max_q, int max_k,
+                        int total_q, int total_k, SeqLayout* lay) {
+  if (!cu_q || !cu_k) return fail(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k are required");
+  FA_TRY(check_i32(cu_q, "cu_seqlens_q"));
+  FA_TRY(check_i32(cu_k, "cu_seqlens_k"));
+  if (nseq < 1) return fail(FA_ERR_INVALID_ARG, "nseq (%d) must be >= 1", nseq);
+  if (max_q < 1 || max_k < 0 || max_q > total_q || max_k > total_k)
+    return fail(FA_ERR_INVALID_ARG,
+                "max_seqlen_q=%d max_seqlen_k=%d must lie in [1, total_q=%d] and [0, total_k=%d]",
+                max_q, max_k, total_q, total_k);
+  lay->grid_b = nseq;
+  lay->longest_q = max_q;
+  lay->longest_k = max_k;
+  lay->cu_q = cu_q;
+  lay->cu_k = cu_k;
+  return FA_OK;
+}
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                 int Hkv, int Sq, int Sk, int d, int causal, float scale,
-                 const int32_t* k_start, const int32_t* k_end, cudaStream_t stream) {
-  FA_TRY(check_sizes(B, Hq, Hkv, Sq, Sk, d));
+fa_status check_key_bits(const uint32_t* bits) {
+  if (bits && !aligned16(bits))
+    return fail(FA_ERR_INVALID_ARG, "key_mask_bits is not 16-byte aligned");
+  return FA_OK;
+}
+
+fa_status fwd_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                     const SeqLayout& lay, const uint32_t* key_bits, cudaStream_t stream) {
   FA_TRY(check_ptr(q, "q"));
   FA_TRY(check_ptr(k, "k"));
   FA_TRY(check_ptr(v, "v"));
   FA_TRY(check_ptr(o, "o"));
   FA_TRY(check_ptr(lse, "lse", true));
-  FA_TRY(check_i32(k_start, "k_start"));
-  FA_TRY(check_i32(k_end, "k_end"));
+  FA_TRY(check_key_bits(key_bits));
   if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale is not finite");
   FA_TRY(check_device());
 
@@ -182,8 +212,12 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   fa::FwdParams p{};
   p.o = o;
   p.lse = lse;
-  p.k_start = k_start;
-  p.k_end = k_end;
+  p.k_start = lay.k_start;
+  p.k_end = lay.k_end;
+  p.cu_q = lay.cu_q;
+  p.cu_k = lay.cu_k;
+  p.key_bits = key_bits;
+  p.mask_words = static_cast<int>(fa_key_mask_words(Sk));
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -191,13 +225,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.Sk = Sk;
   p.group = Hq / Hkv;
   p.pack_heads = (p.group % 2 == 0) ? 1 : 0;
-  const int n_rb = (Sq + fa::kTileM - 1) / fa::kTileM;
+  const int n_rb = (lay.longest_q + fa::kTileM - 1) / fa::kTileM;
   if (p.pack_heads) {
     p.n_rbu = n_rb;
-    p.units_per_rbu = B * (Hq / 2);
+    p.units_per_rbu = lay.grid_b * (Hq / 2);
   } else {
     p.n_rbu = (n_rb + 1) / 2;
-    p.units_per_rbu = B * Hq;
+    p.units_per_rbu = lay.grid_b * Hq;
   }
   p.causal = causal ? 1 : 0;
   p.scale = scale;
@@ -208,6 +242,116 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   cudaError_t e = fa::launch_fwd(d, tq, tk, tv, p, stream);
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "fa_fwd launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+fa_status bwd_launch(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                     int Sq, int Sk, int d, int causal, float scale, const SeqLayout& lay,
+                     const uint32_t* key_bits, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+  FA_TRY(check_ptr(q, "q"));
+  FA_TRY(check_ptr(k, "k"));
+  FA_TRY(check_ptr(v, "v"));
+  FA_TRY(check_ptr(o, "o"));
+  FA_TRY(check_ptr(dout, "dout"));
+  FA_TRY(check_ptr(lse, "lse"));
+  FA_TRY(check_ptr(dq, "dq"));
+  FA_TRY(check_ptr(dk, "dk"));
+  FA_TRY(check_ptr(dv, "dv"));
+  FA_TRY(check_key_bits(key_bits));
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale is not finite");
+  const size_t need = fa_bwd_workspace_size(B, Hq, Sq, d);
+  if (!workspace || workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "backward workspace needs %zu bytes, got %zu", need,
+                workspace ? workspace_bytes : size_t(0));
+  FA_TRY(check_ptr(workspace, "workspace"));
+  FA_TRY(check_device());
+
+  CUtensorMap tq, tk, tv, tdo;
+  FA_TRY(make_map(&tq, q, 1L * B * Hq, Sq, d));
+  FA_TRY(make_map(&tk, k, 1L * B * Hkv, Sk, d));
+  FA_TRY(make_map(&tv, v, 1L * B * Hkv, Sk, d));
+  FA_TRY(make_map(&tdo, dout, 1L * B * Hq, Sq, d));
+
+  fa::BwdParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  const size_t rows = static_cast<size_t>(B) * Hq * Sq;
+  p.dq_acc = static_cast<float*>(workspace);
+  p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                     align256(rows * d * sizeof(float)));
+  p.k_start = lay.k_start;
+  p.k_end = lay.k_end;
+  p.cu_q = lay.cu_q;
+  p.cu_k = lay.cu_k;
+  p.key_bits = key_bits;
+  p.mask_words = static_cast<int>(fa_key_mask_words(Sk));
+  p.grid_b = lay.grid_b;
+  p.n_kt = (lay.longest_k + fa::kTileN - 1) / fa::kTileN;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.group = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  if (1LL * p.n_kt * p.grid_b * Hkv >= (1LL << 31))
+    return fail(FA_ERR_INVALID_ARG, "grid too large");
+  CUtensorMap tdq;
+  FA_TRY(make_map_acc(&tdq, p.dq_acc, 1L * B * Hq, Sq, d));
+  cudaError_t e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "fa_bwd launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                 const int32_t* k_start, const int32_t* k_end, cudaStream_t stream) {
+  return fa_fwd_masked(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, k_start, k_end,
+                       nullptr, stream);
+}
+
+fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                        const int32_t* k_start, const int32_t* k_end,
+                        const uint32_t* key_mask_bits, cudaStream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, Sq, Sk, d));
+  FA_TRY(check_i32(k_start, "k_start"));
+  FA_TRY(check_i32(k_end, "k_end"));
+  SeqLayout lay{};
+  lay.grid_b = B;
+  lay.longest_q = Sq;
+  lay.longest_k = Sk;
+  lay.k_start = k_start;
+  lay.k_end = k_end;
+  return fwd_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, lay, key_mask_bits,
+                    stream);
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                        int Hkv, int d, int causal, float scale, const uint32_t* key_mask_bits,
+                        cudaStream_t stream) {
+  FA_TRY(check_sizes(1, Hq, Hkv, total_q, total_k, d));
+  SeqLayout lay{};
+  FA_TRY(varlen_layout(cu_seqlens_q, cu_seqlens_k, nseq, max_seqlen_q, max_seqlen_k, total_q,
+                       total_k, &lay));
+  return fwd_launch(q, k, v, o, lse, 1, Hq, Hkv, total_q, total_k, d, causal, scale, lay,
+                    key_mask_bits, stream);
 }
 
 size_t fa_decode_workspace_size(int B, int Hq, int Sk_max, int d) {
@@ -273,61 +417,60 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int Sk, int d, int causal, float scale, const int32_t* k_start,
                  const int32_t* k_end, void* workspace, size_t workspace_bytes,
                  cudaStream_t stream) {
+  return fa_bwd_masked(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale,
+                       k_start, k_end, nullptr, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_masked(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                        const int32_t* k_start, const int32_t* k_end,
+                        const uint32_t* key_mask_bits, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
   FA_TRY(check_sizes(B, Hq, Hkv, Sq, Sk, d));
-  FA_TRY(check_ptr(q, "q"));
-  FA_TRY(check_ptr(k, "k"));
-  FA_TRY(check_ptr(v, "v"));
-  FA_TRY(check_ptr(o, "o"));
-  FA_TRY(check_ptr(dout, "dout"));
-  FA_TRY(check_ptr(lse, "lse"));
-  FA_TRY(check_ptr(dq, "dq"));
-  FA_TRY(check_ptr(dk, "dk"));
-  FA_TRY(check_ptr(dv, "dv"));
   FA_TRY(check_i32(k_start, "k_start"));
   FA_TRY(check_i32(k_end, "k_end"));
-  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale is not finite");
-  const size_t need = fa_bwd_workspace_size(B, Hq, Sq, d);
-  if (!workspace || workspace_bytes < need)
-    return fail(FA_ERR_WORKSPACE, "backward workspace needs %zu bytes, got %zu", need,
-                workspace ? workspace_bytes : size_t(0));
-  FA_TRY(check_ptr(workspace, "workspace"));
+  SeqLayout lay{};
+  lay.grid_b = B;
+  lay.longest_q = Sq;
+  lay.longest_k = Sk;
+  lay.k_start = k_start;
+  lay.k_end = k_end;
+  return bwd_launch(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale, lay,
+                    key_mask_bits, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                        int Hkv, int d, int causal, float scale, const uint32_t* key_mask_bits,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_sizes(1, Hq, Hkv, total_q, total_k, d));
+  SeqLayout lay{};
+  FA_TRY(varlen_layout(cu_seqlens_q, cu_seqlens_k, nseq, max_seqlen_q, max_seqlen_k, total_q,
+                       total_k, &lay));
+  return bwd_launch(q, k, v, o, dout, lse, dq, dk, dv, 1, Hq, Hkv, total_q, total_k, d, causal,
+                    scale, lay, key_mask_bits, workspace, workspace_bytes, stream);
+}
+
+size_t fa_key_mask_words(int Sk) {
+  if (Sk < 1) return 0;
+  return static_cast<size_t>((Sk + fa::kTileN - 1) / fa::kTileN) * (fa::kTileN / 32);
+}
+
+fa_status fa_pack_key_mask(const uint8_t* mask, uint32_t* bits, int rows, int Sk,
+                           cudaStream_t stream) {
+  if (rows < 1 || Sk < 1)
+    return fail(FA_ERR_INVALID_ARG, "fa_pack_key_mask: rows=%d Sk=%d must be >= 1", rows, Sk);
+  if (!mask) return fail(FA_ERR_INVALID_ARG, "fa_pack_key_mask: mask is NULL");
+  FA_TRY(check_ptr(bits, "bits"));
+  const size_t words = fa_key_mask_words(Sk);
+  if (static_cast<double>(rows) * words * 32 >= 2147483648.0)
+    return fail(FA_ERR_INVALID_ARG, "fa_pack_key_mask: mask too large");
   FA_TRY(check_device());
-
-  CUtensorMap tq, tk, tv, tdo;
-  FA_TRY(make_map(&tq, q, 1L * B * Hq, Sq, d));
-  FA_TRY(make_map(&tk, k, 1L * B * Hkv, Sk, d));
-  FA_TRY(make_map(&tv, v, 1L * B * Hkv, Sk, d));
-  FA_TRY(make_map(&tdo, dout, 1L * B * Hq, Sq, d));
-
-  fa::BwdParams p{};
-  p.q = q;
-  p.k = k;
-  p.v = v;
-  p.o = o;
-  p.dout = dout;
-  p.lse = lse;
-  p.dq = dq;
-  p.dk = dk;
-  p.dv = dv;
-  const size_t rows = static_cast<size_t>(B) * Hq * Sq;
-  p.dq_acc = static_cast<float*>(workspace);
-  p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                     align256(rows * d * sizeof(float)));
-  p.k_start = k_start;
-  p.k_end = k_end;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.Sq = Sq;
-  p.Sk = Sk;
-  p.group = Hq / Hkv;
-  p.causal = causal ? 1 : 0;
-  p.scale = scale;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-  CUtensorMap tdq;
-  FA_TRY(make_map_acc(&tdq, p.dq_acc, 1L * B * Hq, Sq, d));
-  cudaError_t e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, stream);
-  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "fa_bwd launch: %s", cudaGetErrorString(e));
+  cudaError_t e = fa::launch_pack_key_mask(mask, bits, rows, Sk, static_cast<int>(words), stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "fa_pack_key_mask launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -144,20 +144,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- work unit: key tile (heavy first under the causal rule), KV head, batch
-  const int bh = blockIdx.x % (p.B * p.Hkv);
-  const int kt = blockIdx.x / (p.B * p.Hkv);
+  const int bh = blockIdx.x % (p.grid_b * p.Hkv);
+  const int kt = blockIdx.x / (p.grid_b * p.Hkv);
   const int b = bh / p.Hkv;
   const int hk = bh % p.Hkv;
-  const int c0 = kt * kTileN;
-  int klo = p.k_start ? p.k_start[b] : 0;
-  int kend = p.k_end ? p.k_end[b] : p.Sk;
-  klo = max(0, min(klo, p.Sk));
-  kend = max(0, min(kend, p.Sk));
-  const int off = p.Sk - p.Sq;
-  const int n_qt_all = (p.Sq + kTileM - 1) / kTileM;
+  // This unit's queries: logical rows [0, sq) from packed row qb of tensor
+  // batch bz; its keys [c0, c0 + 128) and the visible interval [klo, kend)
+  // are in the K/V tensor's row coordinates, and keys at or past kseq belong
+  // to another sequence (never stored).
+  int sq = p.Sq, qb = 0, bz = b, klo, kend, kseq, off, c0;
+  if (p.cu_q) {  // packed ragged: b is the sequence
+    qb = max(0, min(p.cu_q[b], p.Sq));
+    sq = max(0, min(p.cu_q[b + 1], p.Sq) - qb);
+    klo = max(0, min(p.cu_k[b], p.Sk));
+    kend = max(klo, min(p.cu_k[b + 1], p.Sk));
+    kseq = kend;
+    off = kend - sq;
+    c0 = klo + kt * kTileN;
+    bz = 0;
+  } else {
+    klo = p.k_start ? p.k_start[b] : 0;
+    kend = p.k_end ? p.k_end[b] : p.Sk;
+    klo = max(0, min(klo, p.Sk));
+    kend = max(0, min(kend, p.Sk));
+    kseq = p.Sk;
+    off = p.Sk - p.Sq;
+    c0 = kt * kTileN;
+  }
+  if (c0 >= kseq) return;  // key tile past the end of its sequence (whole CTA)
+  const int n_qt_all = (sq + kTileM - 1) / kTileM;
   int qt_lo = 0;
   if (p.causal) qt_lo = max(0, c0 - off) / kTileM;  // first query row that sees key c0
-  const bool keys_live = (c0 < kend) && (c0 + kTileN > klo) && (!p.causal || c0 - off < p.Sq);
+  const bool keys_live = (c0 < kend) && (c0 + kTileN > klo) && (!p.causal || c0 - off < sq);
   const int n_qt = keys_live ? max(0, n_qt_all - qt_lo) : 0;
   const int n_it = n_qt * p.group;
 
@@ -204,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
       tma_prefetch_desc(&tdo);
-      const int zkv = b * p.Hkv + hk;
+      const int zkv = bz * p.Hkv + hk;
       mbar_arrive_expect_tx(&s.kv_full, 2 * NB * kBoxBytes);
       for (int cb = 0; cb < NB; ++cb) {
         tma_load_3d(s.k[cb], &tk, &s.kv_full, cb * 64, c0, zkv);
@@ -217,11 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (use > 0 && !mbar_wait(&s.q_empty[st], (use - 1) & 1, abort_flag, kSiteQEmpty)) break;
         const int g = it / n_qt;
         const int q0 = (qt_lo + it % n_qt) * kTileM;
-        const int zq = b * p.Hq + hk * p.group + g;
+        const int zq = bz * p.Hq + hk * p.group + g;
         mbar_arrive_expect_tx(&s.q_full[st], 2 * NB * kBoxBytes);
         for (int cb = 0; cb < NB; ++cb) {
-          tma_load_3d(s.q[st][cb], &tq, &s.q_full[st], cb * 64, q0, zq);
-          tma_load_3d(s.dout[st][cb], &tdo, &s.q_full[st], cb * 64, q0, zq);
+          tma_load_3d(s.q[st][cb], &tq, &s.q_full[st], cb * 64, qb + q0, zq);
+          tma_load_3d(s.dout[st][cb], &tdo, &s.q_full[st], cb * 64, qb + q0, zq);
         }
         issued = it + 1;
       }
@@ -312,7 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = grp * 32 + lane;    // key row in the tile = TMEM lane
     const int key = c0 + row;
     const uint32_t lane_off = static_cast<uint32_t>(grp * 32) << 16;
-    const bool key_in = key >= klo && key < kend;
+    bool key_in = key >= klo && key < kend;
+    if (p.key_bits && key_in) {
+      const uint32_t w = __ldg(p.key_bits + static_cast<size_t>(bz) * p.mask_words + key / 32);
+      key_in = (w >> (key & 31)) & 1u;
+    }
     const float c = p.scale_log2;
     const uint32_t ds_base = smem_u32(s.ds[0]);
     bool ok = true;
@@ -330,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // packed FMA / add per pair; rows without keys get nl = -inf (p = 0)
         const int qi = q0 + row;
         float nl = neg_inf(), nd = 0.f;
-        if (qi < p.Sq) {
-          const size_t ri = (static_cast<size_t>(b) * p.Hq + h) * p.Sq + qi;
+        if (qi < sq) {
+          const size_t ri = (static_cast<size_t>(bz) * p.Hq + h) * p.Sq + qb + qi;
           const float lse = p.lse[ri];
           nl = (lse == neg_inf()) ? neg_inf() : -lse * 1.4426950408889634f;
           nd = -p.delta[ri];
@@ -421,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp-uniform: the TMEM loads below are warp-collective, only the stores
     // depend on the lane's key
     if (ok && !warp_aborted(abort_flag)) {
-      const bool store = key < p.Sk;
-      const size_t kr = (static_cast<size_t>(b) * p.Hkv + hk) * p.Sk + key;
+      const bool store = key < kseq;
+      const size_t kr = (static_cast<size_t>(bz) * p.Hkv + hk) * p.Sk + key;
       __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
       __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
 #pragma unroll
@@ -494,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
 #pragma unroll
         for (int bx = 0; bx < D / 32; ++bx)
-          tma_reduce_add_3d(&tdq, region + bx * 4096, bx * 32, q0 + wq * 32, b * p.Hq + h);
+          tma_reduce_add_3d(&tdq, region + bx * 4096, bx * 32, qb + q0 + wq * 32, bz * p.Hq + h);
         bulk_commit_group();
         bulk_wait_read0();
         mbar_arrive(&s.q_empty[st]);
@@ -531,13 +553,14 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   fa_bwd_pre<D><<<static_cast<unsigned int>((pre_threads + 255) / 256), 256, 0, stream>>>(p, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int n_kt = (p.Sk + kTileN - 1) / kTileN;
-  const unsigned int grid = static_cast<unsigned int>(n_kt) * p.B * p.Hkv;
-  hook_before(stream);
-  fa_bwd_main<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, p);
-  hook_after(stream);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  const unsigned int grid = static_cast<unsigned int>(p.n_kt) * p.grid_b * p.Hkv;
+  if (grid > 0) {  // packed sequences that all lack keys: dQ stays zero
+    hook_before(stream);
+    fa_bwd_main<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, p);
+    hook_after(stream);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const long long n4 = rows * D / 4;
   fa_bwd_convert<<<static_cast<unsigned int>((n4 + 255) / 256), 256, 0, stream>>>(p, n4);
   return cudaGetLastError();

@@ -87,6 +87,16 @@ __device__ __forceinline__ void mask_scores(uint32_t (&sr)[kTileN], int c0, int 
   }
 }
 
+// Scores of keys whose visibility bit is clear become -inf; bit jj of the
+// 128-bit word group kb stands for key c0 + jj.
+template <int FIRST, int COUNT>
+__device__ __forceinline__ void mask_key_bits(uint32_t (&sr)[kTileN], uint4 kb) {
+  const uint32_t w[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+  for (int jj = FIRST; jj < FIRST + COUNT; ++jj)
+    if (!((w[jj >> 5] >> (jj & 31)) & 1u)) sr[jj] = 0xff800000u;
+}
+
 // Weights 2^(s*c - mc) of the 64 scores sr[64*HALF, +64) (nmc2 holds -mc
 // twice), rounded to bf16 pairs and stored to TMEM columns [32*HALF, +32)
 // from t_p.  sum2 gathers the fp32 weights (for l); sr_lo/sr_hi gather the
@@ -149,17 +159,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     r0 = rbu * 2 * kTileM;
     r1 = r0 + kTileM;
   }
-  const bool active1 = r1 < p.Sq;
+  // This unit's rows: logical rows [0, sq) start at packed row qb of tensor
+  // batch bz.  Keys [klo, kend) are in the K/V tensor's own row coordinates.
+  int sq = p.Sq, qb = 0, bz = b, klo, kend, off;
+  if (p.cu_q) {  // packed ragged: b is the sequence
+    qb = max(0, min(p.cu_q[b], p.Sq));
+    sq = max(0, min(p.cu_q[b + 1], p.Sq) - qb);
+    klo = max(0, min(p.cu_k[b], p.Sk));
+    kend = max(klo, min(p.cu_k[b + 1], p.Sk));
+    off = kend - sq;  // bottom-right causal alignment within the sequence
+    bz = 0;
+  } else {
+    klo = p.k_start ? p.k_start[b] : 0;
+    kend = p.k_end ? p.k_end[b] : p.Sk;
+    klo = max(0, min(klo, p.Sk));
+    kend = max(0, min(kend, p.Sk));
+    off = p.Sk - p.Sq;  // bottom-right causal alignment
+  }
+  if (r0 >= sq) return;  // row block past the end of its sequence (whole CTA)
+  const bool active1 = r1 < sq;
   const int hk = h0 / p.group;
-
-  int klo = p.k_start ? p.k_start[b] : 0;
-  int kend = p.k_end ? p.k_end[b] : p.Sk;
-  klo = max(0, min(klo, p.Sk));
-  kend = max(0, min(kend, p.Sk));
-  const int off = p.Sk - p.Sq;  // bottom-right causal alignment
+  const uint32_t* kbits = p.key_bits ? p.key_bits + static_cast<size_t>(bz) * p.mask_words : nullptr;
   int khi = kend;
   if (p.causal) {
-    const int last_row = min((active1 ? r1 : r0) + kTileM - 1, p.Sq - 1);
+    const int last_row = min((active1 ? r1 : r0) + kTileM - 1, sq - 1);
     khi = min(khi, last_row + off + 1);
   }
   int j0 = 0, n_tiles = 0;
@@ -202,10 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t keep = policy_evict_last();
       mbar_arrive_expect_tx(&s.bar_q, (active1 ? 2 : 1) * NB * kBoxBytes);
       for (int cb = 0; cb < NB; ++cb) {
-        tma_load_3d(s.q[0][cb], &tq, &s.bar_q, cb * 64, r0, b * p.Hq + h0);
-        if (active1) tma_load_3d(s.q[1][cb], &tq, &s.bar_q, cb * 64, r1, b * p.Hq + h1);
+        tma_load_3d(s.q[0][cb], &tq, &s.bar_q, cb * 64, qb + r0, bz * p.Hq + h0);
+        if (active1) tma_load_3d(s.q[1][cb], &tq, &s.bar_q, cb * 64, qb + r1, bz * p.Hq + h1);
       }
-      const int zkv = b * p.Hkv + hk;
+      const int zkv = bz * p.Hkv + hk;
       int k_issued = 0, v_issued = 0;  // tiles whose loads were issued
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % NS;
@@ -334,6 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need_mask = (c0 < klo) || (c0 + kTileN > khi_row);
         const bool masked_tile = __any_sync(0xffffffffu, need_mask);
         if (masked_tile) mask_scores<0, kTileN>(sr, c0, klo, khi_row);
+        // key visibility bits of this tile (the same 128 bits for every row)
+        uint4 kb = make_uint4(~0u, ~0u, ~0u, ~0u);
+        if (kbits) kb = __ldg(reinterpret_cast<const uint4*>(kbits + c0 / 32));
+        const bool bit_masked = (kb.x & kb.y & kb.z & kb.w) != ~0u;
+        if (bit_masked) mask_key_bits<0, kTileN>(sr, kb);
         // Fast path: weights relative to the running max as it stands.  The
         // max only keeps the weights finite, and the fp32 tile sum (needed for
         // l anyway) bounds every weight of the row, so the tile is checked
@@ -368,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           tmem_wait_st();  // fast-path P stores land before they are rewritten
           if (masked_tile) mask_scores<0, kTileN / 2>(sr, c0, klo, khi_row);
+          if (bit_masked) mask_key_bits<0, kTileN / 2>(sr, kb);
           // row max: 8 independent chains of 3-input max
           float mx8[8];
 #pragma unroll
@@ -429,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (((t == 0) || active1) && ok && !warp_aborted(abort_flag)) {
       const bool live = l > 0.f;
       const float inv = live ? 1.f / lr : 0.f;
-      const bool in_range = i < p.Sq;
-      const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Sq + i;
+      const bool in_range = i < sq;
+      const size_t row = (static_cast<size_t>(bz) * p.Hq + h) * p.Sq + qb + i;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {

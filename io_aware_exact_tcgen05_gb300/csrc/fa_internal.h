@@ -36,6 +36,15 @@ struct FwdParams {
   float* lse;          // fp32 [B,Hq,Sq] or nullptr
   const int32_t* k_start;
   const int32_t* k_end;
+  // Packed ragged sequences (B = 1, Sq/Sk = packed totals): sequence s owns
+  // rows [cu_q[s], cu_q[s+1]) and keys [cu_k[s], cu_k[s+1]); the grid's batch
+  // index is the sequence.  nullptr for the batched layout.
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  // Optional key visibility bits: bit (j & 31) of word [row * mask_words + j / 32],
+  // row = batch row (or 0 for packed keys); nullptr = every key visible.
+  const uint32_t* key_bits;
+  int mask_words;
   int B, Hq, Hkv, Sq, Sk;
   int group;           // Hq / Hkv
   int pack_heads;      // 1: a CTA's two query tiles are two heads of one KV group
@@ -85,11 +94,21 @@ struct BwdParams {
   float* delta;         // fp32 [B,Hq,Sq] workspace: D_i
   const int32_t* k_start;
   const int32_t* k_end;
+  const int32_t* cu_q;     // packed ragged sequences, as in FwdParams (nullptr: batched)
+  const int32_t* cu_k;
+  const uint32_t* key_bits;  // optional key visibility bits, as in FwdParams
+  int mask_words;
+  int grid_b;  // units along the grid's batch axis: B, or the sequence count when packed
+  int n_kt;    // key tiles per unit: ceil(Sk / 128), or ceil(longest sequence's keys / 128)
   int B, Hq, Hkv, Sq, Sk, group;
   int causal;
   float scale;
   float scale_log2;
 };
+
+// bits[r][words] = packed (mask[r][Sk] != 0), zero past Sk.
+cudaError_t launch_pack_key_mask(const uint8_t* mask, uint32_t* bits, int rows, int Sk, int words,
+                                 cudaStream_t stream);
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,

@@ -105,3 +105,47 @@ def _load_missing(tmp_path):
         fa.load_library(str(tmp_path / "nope.so"))
     finally:
         fa._lib = saved
+
+
+def _fwd_varlen(lib, cu_q=16, cu_k=16, nseq=2, max_q=8, max_k=8, total_q=16, total_k=16, Hq=2,
+                Hkv=2, d=128, bits=None):
+    return lib.fa_fwd_varlen(P(16), P(16), P(16), P(16), None, P(cu_q), P(cu_k), nseq, max_q,
+                             max_k, total_q, total_k, Hq, Hkv, d, 1, ctypes.c_float(0.1),
+                             P(bits), None)
+
+
+def test_varlen_and_mask_validation_before_any_device_call(lib):
+    assert _fwd_varlen(lib, cu_q=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_varlen(lib, cu_k=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_varlen(lib, cu_q=18) == fa.FA_ERR_INVALID_ARG  # not 4-byte aligned
+    assert _fwd_varlen(lib, nseq=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_varlen(lib, max_q=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_varlen(lib, max_q=17) == fa.FA_ERR_INVALID_ARG  # longer than the packed total
+    assert _fwd_varlen(lib, max_k=-1) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_varlen(lib, total_k=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd_varlen(lib, d=80) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd_varlen(lib, bits=20) == fa.FA_ERR_INVALID_ARG  # bits not 16-byte aligned
+    st = lib.fa_fwd_masked(P(16), P(16), P(16), P(16), None, 1, 2, 2, 8, 8, 128, 0,
+                           ctypes.c_float(0.1), None, None, P(24), None)
+    assert st == fa.FA_ERR_INVALID_ARG
+    st = lib.fa_bwd_varlen(P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16),
+                           None, P(16), 2, 8, 8, 16, 16, 2, 2, 128, 1, ctypes.c_float(0.1), None,
+                           P(256), 1 << 20, None)
+    assert st == fa.FA_ERR_INVALID_ARG
+    st = lib.fa_bwd_masked(P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16),
+                           1, 2, 2, 8, 8, 128, 1, ctypes.c_float(0.1), None, None, P(16),
+                           P(256), 16, None)
+    assert st == fa.FA_ERR_WORKSPACE
+    assert lib.fa_pack_key_mask(P(16), P(16), 0, 8, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_pack_key_mask(None, P(16), 1, 8, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_pack_key_mask(P(16), P(20), 1, 8, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_key_mask_words(lib):
+    # 4 words (one 128-key tile) per started tile, so every tile's bits are one
+    # aligned 16-byte load
+    assert fa.fa_key_mask_words(1) == 4
+    assert fa.fa_key_mask_words(128) == 4
+    assert fa.fa_key_mask_words(129) == 8
+    assert fa.fa_key_mask_words(8192) == 256
+    assert fa.fa_key_mask_words(0) == 0
