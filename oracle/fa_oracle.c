@@ -37,6 +37,19 @@
  * query head h reads KV head h / (Hq/Hkv), and dK/dV of a KV head sum over
  * the query heads that read it.
  *
+ * Dropout on the attention weights (FlashAttention_01 page, "why the
+ * backward can recompute" and "interface and implementation constraints":
+ * the random mask is part of the forward/backward contract and must be
+ * reproduced element by element).  With probability p_drop, weight (i, j)
+ * is dropped and the kept ones are scaled by 1 / (1 - p_drop):
+ *   O_i   = u_i / l_i,  u_i = sum_vis exp(s_ij - m) keep_ij / (1 - p) v_j
+ *   (m, l and LSE are those of the undropped weights)
+ *   dP_ij = keep_ij / (1 - p) <dO_i, v_j>,  dV_j = sum_i p_ij keep_ij / (1 - p) dO_i
+ * keep_ij comes from Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel
+ * random numbers: as easy as 1, 2, 3", SC 2011) with counter
+ * (j / 4, i, b * Hq + h, offset) and key (seed low word, seed high word):
+ * keep_ij <=> word (j mod 4) >= floor(p * 2^32).
+ *
  * Inputs are either fp64 arrays or bf16 bit patterns (uint16); a bf16 value
  * is widened to fp64 exactly.  Layout is [B, H, S, d], d innermost.
  * OpenMP only distributes independent rows (or independent key rows for
@@ -63,6 +76,74 @@ typedef struct {
   const void* p;
   int bf16;
 } src_t;
+
+/* ---- Philox4x32-10, restated from the SC 2011 paper ----------------------
+ * state: four 32-bit counter words and a two-word key.  One round maps
+ * (c0, c1, c2, c3) to (hi(B*c2) ^ c1 ^ k0, lo(B*c2), hi(A*c0) ^ c3 ^ k1,
+ * lo(A*c0)) with the paper's multipliers A, B; the key is advanced by the
+ * paper's Weyl constants before every round but the first. */
+static void philox4x32_10(const uint32_t ctr[4], uint32_t k0, uint32_t k1, uint32_t out[4]) {
+  const uint64_t A = 0xD2511F53u, B = 0xCD9E8D57u;
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint64_t p0 = A * (uint64_t)c0;
+    const uint64_t p1 = B * (uint64_t)c2;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    const uint32_t n1 = (uint32_t)p1;
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    const uint32_t n3 = (uint32_t)p0;
+    c0 = n0;
+    c1 = n1;
+    c2 = n2;
+    c3 = n3;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+void oracle_philox4x32_10(const uint32_t* ctr, uint32_t k0, uint32_t k1, uint32_t* out) {
+  philox4x32_10(ctr, k0, k1, out);
+}
+
+typedef struct {
+  int on;
+  uint32_t thr;          /* floor(p * 2^32): keep iff the word is >= thr */
+  double keep_scale;     /* 1 / (1 - p) */
+  uint32_t seed_lo, seed_hi, offset;
+} drop_t;
+
+static drop_t make_drop(double p, unsigned long long seed, unsigned int offset) {
+  drop_t d;
+  d.on = p > 0.0;
+  d.thr = d.on ? (uint32_t)floor(p * 4294967296.0) : 0u;
+  d.keep_scale = d.on ? 1.0 / (1.0 - p) : 1.0;
+  d.seed_lo = (uint32_t)(seed & 0xffffffffull);
+  d.seed_hi = (uint32_t)(seed >> 32);
+  d.offset = offset;
+  return d;
+}
+
+/* keep_ij / (1 - p) for query row i of query head bh (= b * Hq + h), key j */
+static double drop_factor(const drop_t* d, long bh, long i, long j) {
+  if (!d || !d->on) return 1.0;
+  const uint32_t ctr[4] = {(uint32_t)(j >> 2), (uint32_t)i, (uint32_t)bh, d->offset};
+  uint32_t w[4];
+  philox4x32_10(ctr, d->seed_lo, d->seed_hi, w);
+  return (w[j & 3] >= d->thr) ? d->keep_scale : 0.0;
+}
+
+/* 1 when weight (i, j) of query head bh is kept, 0 when dropped */
+int oracle_dropout_keep(double p, unsigned long long seed, unsigned int offset, long bh, long i,
+                        long j) {
+  const drop_t d = make_drop(p, seed, offset);
+  return drop_factor(&d, bh, i, j) != 0.0;
+}
 
 static double ld(src_t s, long idx) {
   if (s.bf16) return bf16_bits_to_double(((const uint16_t*)s.p)[idx]);
@@ -98,8 +179,8 @@ static void key_range(const int* k_start, const int* k_end, long b, long Sk, lon
  */
 static void row_attention(const double* qrow, src_t k, long kbase, src_t v, long vbase,
                           long n, long d, double scale, long i, long Sq, int causal,
-                          long ks, long ke, const unsigned char* km, double* s,
-                          double* m_out, double* l_out,
+                          long ks, long ke, const unsigned char* km, const drop_t* dr,
+                          long bh, double* s, double* m_out, double* l_out,
                           double* u, double* o, double* lse_out) {
   double m = -INFINITY;
   long nvis = 0;
@@ -124,7 +205,8 @@ static void row_attention(const double* qrow, src_t k, long kbase, src_t v, long
     if (!is_visible(i, j, Sq, n, causal, ks, ke, km)) continue;
     double e = exp(s[j] - m);
     l += e;
-    for (long c = 0; c < d; ++c) u[c] += e * ld(v, vbase + j * d + c);
+    const double ed = e * drop_factor(dr, bh, i, j);
+    for (long c = 0; c < d; ++c) u[c] += ed * ld(v, vbase + j * d + c);
   }
   *m_out = m;
   *l_out = l;
@@ -141,7 +223,7 @@ int oracle_row_state(const double* q, const double* k, const double* v, long n, 
   double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
   if (!s) return 1;
   src_t ks = {k, 0}, vs = {v, 0};
-  row_attention(q, ks, 0, vs, 0, n, d, scale, 0, 1, 0, 0, n, NULL, s, m, l, u, o, lse);
+  row_attention(q, ks, 0, vs, 0, n, d, scale, 0, 1, 0, 0, n, NULL, NULL, 0, s, m, l, u, o, lse);
   free(s);
   return 0;
 }
@@ -156,9 +238,11 @@ int oracle_row_state(const double* q, const double* k, const double* v, long n, 
 int oracle_fwd(const void* q, const void* k, const void* v, int in_bf16, long B, long Hq,
                long Hkv, long Sq, long Sk, long d, int causal, double scale,
                const int* k_start, const int* k_end, const unsigned char* key_mask,
+               double p_drop, unsigned long long seed, unsigned int offset,
                long nrows, const long* rows,
                double* o, double* lse, double* m_out, double* l_out) {
   if (Hkv <= 0 || Hq % Hkv != 0) return 1;
+  const drop_t dr = make_drop(p_drop, seed, offset);
   const long group = Hq / Hkv;
   const long total = rows ? nrows : B * Hq * Sq;
   src_t qs = {q, in_bf16}, kk = {k, in_bf16}, vv = {v, in_bf16};
@@ -185,7 +269,8 @@ int oracle_fwd(const void* q, const void* k, const void* v, int in_bf16, long B,
         const long kvbase = (b * Hkv + hk) * Sk * d;
         double m, l;
         row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke,
-                      mask_row(key_mask, b, Sk), s, &m, &l, u, o + r * d, lse + r);
+                      mask_row(key_mask, b, Sk), &dr, b * Hq + h, s, &m, &l, u, o + r * d,
+                      lse + r);
         if (m_out) m_out[r] = m;
         if (l_out) l_out[r] = l;
       }
@@ -204,8 +289,10 @@ int oracle_fwd(const void* q, const void* k, const void* v, int in_bf16, long B,
 int oracle_probs(const void* q, const void* k, const void* v, const void* dout, int in_bf16,
                  long B, long Hq, long Hkv, long Sq, long Sk, long d, int causal,
                  double scale, const int* k_start, const int* k_end,
-                 const unsigned char* key_mask, double* p, double* ds) {
+                 const unsigned char* key_mask, double p_drop, unsigned long long seed,
+                 unsigned int offset, double* p, double* ds) {
   if (Hkv <= 0 || Hq % Hkv != 0) return 1;
+  const drop_t dr = make_drop(p_drop, seed, offset);
   const long group = Hq / Hkv;
   src_t qs = {q, in_bf16}, kk = {k, in_bf16}, vv = {v, in_bf16}, dos = {dout, in_bf16};
   double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
@@ -223,8 +310,8 @@ int oracle_probs(const void* q, const void* k, const void* v, const void* dout, 
         load_row(qs, flat * d, d, qrow);
         double m, l, lse;
         const unsigned char* km = mask_row(key_mask, b, Sk);
-        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, km, s,
-                      &m, &l, u, orow, &lse);
+        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, km, &dr,
+                      b * Hq + h, s, &m, &l, u, orow, &lse);
         double D = 0.0;
         if (ds)
           for (long c = 0; c < d; ++c) D += ld(dos, flat * d + c) * orow[c];
@@ -236,7 +323,7 @@ int oracle_probs(const void* q, const void* k, const void* v, const void* dout, 
           if (ds) {
             double dp = 0.0;
             for (long c = 0; c < d; ++c) dp += ld(dos, flat * d + c) * ld(vv, kvbase + j * d + c);
-            ds[idx] = pij * (dp - D);
+            ds[idx] = pij * (dp * drop_factor(&dr, b * Hq + h, i, j) - D);
           }
         }
       }
@@ -254,9 +341,11 @@ int oracle_probs(const void* q, const void* k, const void* v, const void* dout, 
  */
 int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, int in_bf16,
                long B, long Hq, long Hkv, long Sq, long Sk, long d, int causal, double scale,
-               const int* k_start, const int* k_end, const unsigned char* key_mask, double* dq,
+               const int* k_start, const int* k_end, const unsigned char* key_mask,
+               double p_drop, unsigned long long seed, unsigned int offset, double* dq,
                double* dk, double* dv) {
   if (Hkv <= 0 || Hq % Hkv != 0) return 1;
+  const drop_t dr = make_drop(p_drop, seed, offset);
   const long group = Hq / Hkv;
   const long nrow = B * Hq * Sq;
   src_t qs = {q, in_bf16}, kk = {k, in_bf16}, vv = {v, in_bf16}, dos = {dout, in_bf16};
@@ -290,8 +379,8 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
         load_row(dos, flat * d, d, dorow);
         double lse;
         const unsigned char* km = mask_row(key_mask, b, Sk);
-        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, km, s,
-                      &M[flat], &L[flat], u, orow, &lse);
+        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, km, &dr,
+                      b * Hq + h, s, &M[flat], &L[flat], u, orow, &lse);
         double D = 0.0;
         for (long c = 0; c < d; ++c) D += dorow[c] * orow[c];
         Dv[flat] = D;
@@ -303,7 +392,7 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
           const double pij = exp(s[j] - M[flat]) / L[flat];
           double dp = 0.0;
           for (long c = 0; c < d; ++c) dp += dorow[c] * ld(vv, kvbase + j * d + c);
-          const double dsij = pij * (dp - D);
+          const double dsij = pij * (dp * drop_factor(&dr, b * Hq + h, i, j) - D);
           for (long c = 0; c < d; ++c) dqr[c] += scale * dsij * ld(kk, kvbase + j * d + c);
         }
       }
@@ -350,9 +439,10 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
             sij *= scale;
             for (long c = 0; c < d; ++c) dp += ld(dos, flat * d + c) * vrow[c];
             const double pij = exp(sij - M[flat]) / L[flat];
-            const double dsij = pij * (dp - Dv[flat]);
+            const double f = drop_factor(&dr, b * Hq + h, i, j);
+            const double dsij = pij * (dp * f - Dv[flat]);
             for (long c = 0; c < d; ++c) {
-              dvr[c] += pij * ld(dos, flat * d + c);
+              dvr[c] += pij * f * ld(dos, flat * d + c);
               dkr[c] += scale * dsij * ld(qs, flat * d + c);
             }
           }

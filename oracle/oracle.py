@@ -48,12 +48,17 @@ def _load():
             lib = ctypes.CDLL(_LIB)
             P = ctypes.c_void_p
             L = ctypes.c_long
+            D, U64, U32 = ctypes.c_double, ctypes.c_ulonglong, ctypes.c_uint
             lib.oracle_fwd.argtypes = [P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
-                                       ctypes.c_double, P, P, P, L, P, P, P, P, P]
+                                       D, P, P, P, D, U64, U32, L, P, P, P, P, P]
             lib.oracle_bwd.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
-                                       ctypes.c_double, P, P, P, P, P, P]
+                                       D, P, P, P, D, U64, U32, P, P, P]
             lib.oracle_probs.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
-                                         ctypes.c_double, P, P, P, P, P]
+                                         D, P, P, P, D, U64, U32, P, P]
+            lib.oracle_philox4x32_10.argtypes = [P, U32, U32, P]
+            lib.oracle_philox4x32_10.restype = None
+            lib.oracle_dropout_keep.argtypes = [D, U64, U32, L, L, L]
+            lib.oracle_dropout_keep.restype = ctypes.c_int
             lib.oracle_row_state.argtypes = [P, P, P, L, L, ctypes.c_double, P, P, P, P, P]
             for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_probs, lib.oracle_row_state):
                 f.restype = ctypes.c_int
@@ -120,7 +125,8 @@ def num_threads() -> int:
 
 
 def fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, rows=None,
-        return_stats: bool = False, key_mask=None):
+        return_stats: bool = False, key_mask=None, dropout_p: float = 0.0, seed: int = 0,
+        offset: int = 0):
     """Forward O and LSE from the definition (the "Flash Attention" history page
     1.1-1.2; FlashAttention_01 page, online-softmax derivation, masking rule).
 
@@ -129,6 +135,8 @@ def fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, rows=None
     [len(rows), d] / [len(rows)].  Fully masked rows give O=0, LSE=-inf.
     key_mask: optional [B, Sk] booleans; a key whose entry is false is not
     visible to any query of that batch row.
+    dropout_p, seed, offset: dropout on the weights (see dropout_keep); the
+    statistics m, l and LSE are those of the undropped weights.
     """
     qa, bf = _as_input(q)
     ka, bk = _as_input(k)
@@ -149,8 +157,9 @@ def fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, rows=None
     m = np.empty((n,), np.float64) if return_stats else None
     l = np.empty((n,), np.float64) if return_stats else None
     rc = _load().oracle_fwd(_ptr(qa), _ptr(ka), _ptr(va), bf, B, Hq, Hkv, Sq, Sk, d, int(causal),
-                            float(scale), _ptr(ks), _ptr(ke), _ptr(_mask(key_mask, B, Sk)), n,
-                            _ptr(rr), _ptr(o), _ptr(lse), _ptr(m), _ptr(l))
+                            float(scale), _ptr(ks), _ptr(ke), _ptr(_mask(key_mask, B, Sk)),
+                            float(dropout_p), int(seed), int(offset), n, _ptr(rr), _ptr(o),
+                            _ptr(lse), _ptr(m), _ptr(l))
     if rc:
         raise RuntimeError(f"oracle_fwd failed ({rc})")
     if rows is None:
@@ -164,7 +173,8 @@ def fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, rows=None
     return o, lse
 
 
-def bwd(q, k, v, dout, causal: bool, scale: float, k_start=None, k_end=None, key_mask=None):
+def bwd(q, k, v, dout, causal: bool, scale: float, k_start=None, k_end=None, key_mask=None,
+        dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
     """dQ, dK, dV from the definition (FlashAttention_01 page, "why the backward
     can recompute" and the chain-rule section): dV=P^T dO, dP=dO V^T,
     dS=P*(dP-rowsum(dO*O)), dQ=scale dS K, dK=scale dS^T Q; GQA heads summed."""
@@ -179,15 +189,16 @@ def bwd(q, k, v, dout, causal: bool, scale: float, k_start=None, k_end=None, key
     dv = np.empty((B, Hkv, Sk, d), np.float64)
     rc = _load().oracle_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), bf, B, Hq, Hkv, Sq, Sk, d,
                             int(causal), float(scale), _ptr(_i32(k_start, B)),
-                            _ptr(_i32(k_end, B)), _ptr(_mask(key_mask, B, Sk)), _ptr(dq),
-                            _ptr(dk), _ptr(dv))
+                            _ptr(_i32(k_end, B)), _ptr(_mask(key_mask, B, Sk)),
+                            float(dropout_p), int(seed), int(offset), _ptr(dq), _ptr(dk),
+                            _ptr(dv))
     if rc:
         raise RuntimeError(f"oracle_bwd failed ({rc})")
     return dq, dk, dv
 
 
 def probs(q, k, v, causal: bool, scale: float, dout=None, k_start=None, k_end=None,
-          key_mask=None):
+          key_mask=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
     """Dense P [B,Hq,Sq,Sk] and, when dout is given, dS (small problems only)."""
     qa, bf = _as_input(q)
     ka, _ = _as_input(k)
@@ -199,11 +210,28 @@ def probs(q, k, v, causal: bool, scale: float, dout=None, k_start=None, k_end=No
     ds = np.empty((B, Hq, Sq, Sk), np.float64) if dout is not None else None
     rc = _load().oracle_probs(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), bf, B, Hq, Hkv, Sq, Sk, d,
                               int(causal), float(scale), _ptr(_i32(k_start, B)),
-                              _ptr(_i32(k_end, B)), _ptr(_mask(key_mask, B, Sk)), _ptr(p),
-                              _ptr(ds))
+                              _ptr(_i32(k_end, B)), _ptr(_mask(key_mask, B, Sk)),
+                              float(dropout_p), int(seed), int(offset), _ptr(p), _ptr(ds))
     if rc:
         raise RuntimeError(f"oracle_probs failed ({rc})")
     return (p, ds) if dout is not None else p
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 (Salmon et al., SC 2011) of four 32-bit counter words and
+    two 32-bit key words; returns four 32-bit words."""
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32))
+    out = np.zeros(4, np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), int(key[0]) & 0xffffffff, int(key[1]) & 0xffffffff,
+                                 _ptr(out))
+    return out
+
+
+def dropout_keep(p: float, seed: int, offset: int, bh: int, i: int, j: int) -> bool:
+    """Whether weight (query row i, key j) of query head bh = b*Hq + h is kept:
+    word j % 4 of Philox4x32-10 at counter (j // 4, i, bh, offset) under key
+    (seed low 32 bits, seed high 32 bits) is >= floor(p * 2^32)."""
+    return bool(_load().oracle_dropout_keep(float(p), int(seed), int(offset), bh, i, j))
 
 
 def row_state(q, k, v, scale: float):

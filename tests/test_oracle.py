@@ -328,6 +328,75 @@ def test_varlen_equal_lengths_equals_batched():
     assert np.array_equal(lse, lb.transpose(1, 0, 2).reshape(Hq, B * S))
 
 
+# --- dropout with a counter-based mask (FlashAttention_01 page, "why the
+#     backward can recompute" and "interface and implementation constraints":
+#     the element-to-random-number mapping is part of the contract) ---
+
+# Known-answer vectors published with the reference implementation of
+# Philox4x32-10 (Random123, Salmon et al., SC 2011): counter, key -> output.
+PHILOX_KAT = [
+    ([0, 0, 0, 0], [0, 0], [0x6627e8d5, 0xe169c58d, 0xbc57ac4c, 0x9b00dbd8]),
+    ([0xffffffff] * 4, [0xffffffff] * 2, [0x408f276d, 0x41c83b0e, 0xa20bc7c6, 0x6d5451fd]),
+    ([0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344], [0xa4093822, 0x299f31d0],
+     [0xd16cfe09, 0x94fdcceb, 0x5001e420, 0x24126ea1]),
+]
+
+
+@pytest.mark.parametrize("ctr,key,want", PHILOX_KAT)
+def test_philox_known_answers(ctr, key, want):
+    assert [int(x) for x in orc.philox4x32_10(ctr, key)] == want
+
+
+def test_dropout_keep_rate_and_mapping():
+    p, seed, off = 0.3, 0x0123456789ABCDEF, 7
+    keep = np.array([orc.dropout_keep(p, seed, off, bh, i, j)
+                     for bh in range(2) for i in range(60) for j in range(257)])
+    n = keep.size
+    sigma = math.sqrt(n * p * (1 - p))
+    assert abs(keep.sum() - n * (1 - p)) < 5 * sigma
+    # the decision is word j % 4 of the Philox call at counter (j // 4, i, bh, offset)
+    for (bh, i, j) in [(0, 0, 0), (1, 5, 6), (1, 59, 255), (0, 17, 3)]:
+        w = orc.philox4x32_10([j // 4, i, bh, off], [seed & 0xffffffff, seed >> 32])
+        assert orc.dropout_keep(p, seed, off, bh, i, j) == (int(w[j % 4]) >= int(p * 2**32))
+    # p = 0 keeps everything; another seed or offset gives another mask
+    assert all(orc.dropout_keep(0.0, seed, off, 0, 3, j) for j in range(64))
+    a = [orc.dropout_keep(p, seed, off, 0, 3, j) for j in range(256)]
+    assert a != [orc.dropout_keep(p, seed + 1, off, 0, 3, j) for j in range(256)]
+    assert a != [orc.dropout_keep(p, seed, off + 1, 0, 3, j) for j in range(256)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dropout_matches_explicit_mask_in_torch_fp64(causal):
+    B, Hq, Hkv, Sq, Sk, d = 2, 4, 2, 19, 23, 8
+    p, seed, off = 0.25, 99, 3
+    q = _rand((B, Hq, Sq, d), 80)
+    k = _rand((B, Hkv, Sk, d), 81)
+    v = _rand((B, Hkv, Sk, d), 82)
+    do = _rand((B, Hq, Sq, d), 83)
+    scale = 1.0 / math.sqrt(d)
+    keep = torch.tensor([[[[orc.dropout_keep(p, seed, off, b * Hq + h, i, j) for j in range(Sk)]
+                           for i in range(Sq)] for h in range(Hq)] for b in range(B)],
+                        dtype=torch.float64)
+    vis = _mask(Sq, Sk, causal, [0] * B, [Sk] * B, B)
+    qt, kt, vt = (x.clone().requires_grad_() for x in (q, k, v))
+    rep = Hq // Hkv
+    s = torch.einsum("bhid,bhjd->bhij", qt, kt.repeat_interleave(rep, 1)) * scale
+    s = s.masked_fill(~vis, -math.inf)
+    prob = torch.softmax(s, -1)
+    ref = torch.einsum("bhij,bhjd->bhid", prob * keep / (1 - p), vt.repeat_interleave(rep, 1))
+    ref.backward(do)
+    o, lse = orc.fwd(q, k, v, causal, scale, dropout_p=p, seed=seed, offset=off)
+    assert np.abs(o - ref.detach().numpy()).max() < 1e-12
+    assert np.abs(lse - torch.logsumexp(s.detach(), -1).numpy()).max() < 1e-12  # undropped
+    dq, dk, dv = orc.bwd(q, k, v, do, causal, scale, dropout_p=p, seed=seed, offset=off)
+    for mine, theirs in ((dq, qt.grad), (dk, kt.grad), (dv, vt.grad)):
+        assert np.abs(mine - theirs.numpy()).max() < 1e-11
+    # p = 0 is exactly the plain path
+    a = orc.fwd(q, k, v, causal, scale, dropout_p=0.0, seed=seed, offset=off)
+    b_ = orc.fwd(q, k, v, causal, scale)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b_))
+
+
 # --- chain-rule section: central differences on the 2x3x2 masked example ---
 
 def _loss(q, k, v):
