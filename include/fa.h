@@ -35,6 +35,8 @@
  *  * A row with no visible key gets O = 0 and LSE = -inf, and contributes zero
  *    gradient; no -inf - (-inf) is ever evaluated.
  *  * d (head dimension) must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
+ *  * scale must be finite and >= 0 (FA_ERR_INVALID_ARG otherwise); scale 0
+ *    gives uniform weights over the visible keys.
  *  * Calls are asynchronous: they validate, enqueue kernels on `stream` and
  *    return.  A validation failure returns before any launch and writes
  *    nothing.  Launch failures return FA_ERR_CUDA.  fa_last_error_detail()
@@ -167,6 +169,36 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
                         int Hkv, int d, int causal, float scale, const uint32_t* key_mask_bits,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Dropout on the attention weights, with the random mapping fixed as part of
+ * the forward/backward contract (FlashAttention_01 page, "why the backward
+ * can recompute", "interface and implementation constraints" and "training
+ * configuration and misuse boundaries": recomputation needs the same mask,
+ * statistics, scale and dropout mapping).
+ *   O_i = sum_j P_ij * keep_ij / (1 - p) * v_j,  P the undropped softmax;
+ *   LSE is the undropped one (what the backward needs to rebuild P).
+ *   keep_ij <=> word (j mod 4) of Philox4x32-10 (Salmon et al., SC 2011) at
+ *   counter (j / 4, i, b * Hq + h, offset) under key (seed & 0xffffffff,
+ *   seed >> 32) is >= floor(dropout_p * 2^32); i is the query row and j the
+ *   key index within batch row b.
+ * dropout_p must lie in [0, 1) (0 = no dropout); the backward must get the
+ * forward's dropout_p, seed and offset.  Otherwise these are fa_fwd_masked /
+ * fa_bwd_masked (key_mask_bits may be NULL).
+ */
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                         const int32_t* k_start, const int32_t* k_end,
+                         const uint32_t* key_mask_bits, float dropout_p,
+                         unsigned long long seed, unsigned int offset, cudaStream_t stream);
+
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                         const int32_t* k_start, const int32_t* k_end,
+                         const uint32_t* key_mask_bits, float dropout_p,
+                         unsigned long long seed, unsigned int offset, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of device workspace fa_decode needs for a cache of Sk_max positions:
    per (b, query head, split) partial outputs and logsumexps. */

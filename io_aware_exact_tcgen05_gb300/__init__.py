@@ -26,7 +26,8 @@ FA_ERR_TIMEOUT = 5
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_decode", "fa_decode_workspace_size",
             "fa_decode_noalloc", "fa_fwd_masked", "fa_bwd_masked", "fa_fwd_varlen",
-            "fa_bwd_varlen", "fa_key_mask_words", "fa_pack_key_mask", "fa_device_status",
+            "fa_bwd_varlen", "fa_fwd_dropout", "fa_bwd_dropout", "fa_key_mask_words",
+            "fa_pack_key_mask", "fa_device_status",
             "fa_profile_next_launch", "fa_status_string", "fa_last_error_detail", "fa_version")
 
 _lib = None
@@ -57,6 +58,12 @@ def load_library(path: str = LIB_PATH):
     lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P]
     lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P,
                                   P, Z, P]
+    U64, U32 = ctypes.c_ulonglong, ctypes.c_uint
+    lib.fa_fwd_dropout.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, F, U64, U32, P]
+    lib.fa_bwd_dropout.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, F,
+                                   U64, U32, P, Z, P]
+    lib.fa_fwd_dropout.restype = I
+    lib.fa_bwd_dropout.restype = I
     lib.fa_key_mask_words.argtypes = [I]
     lib.fa_key_mask_words.restype = Z
     lib.fa_pack_key_mask.argtypes = [P, P, I, I, P]
@@ -142,11 +149,13 @@ def _mask_bits(key_mask, rows, Sk, stream):
 
 
 def fa_fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, o=None, lse=None,
-           stream=None, key_mask=None):
+           stream=None, key_mask=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
     """O, LSE = attention(q, k, v) via the library's fa_fwd (see include/fa.h).
     q [B,Hq,Sq,d], k/v [B,Hkv,Sk,d] bf16 CUDA tensors; k_start/k_end optional
     int32 [B] CUDA tensors; key_mask optional [B, Sk] bool CUDA tensor (or its
-    fa_pack_key_mask words), giving fa_fwd_masked.  Returns (o, lse)."""
+    fa_pack_key_mask words), giving fa_fwd_masked.  dropout_p > 0 (taken as
+    float32) gives fa_fwd_dropout with the given seed and offset.
+    Returns (o, lse)."""
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, 4)
@@ -160,7 +169,13 @@ def fa_fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, o=None
         if t is not None:
             _need(t, n, torch.int32, 1)
     bits = _mask_bits(key_mask, B, Sk, stream)
-    if bits is None:
+    if dropout_p > 0.0:
+        st = lib.fa_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq,
+                                Sk, d, int(bool(causal)), float(scale), _ptr(k_start),
+                                _ptr(k_end), _ptr(bits), float(dropout_p), int(seed),
+                                int(offset), _stream(stream))
+        _check(st, "fa_fwd_dropout")
+    elif bits is None:
         st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
                         int(bool(causal)), float(scale), _ptr(k_start), _ptr(k_end),
                         _stream(stream))
@@ -178,9 +193,11 @@ def fa_bwd_workspace_size(B, Hq, Sq, d) -> int:
 
 
 def fa_bwd(q, k, v, o, dout, lse, causal: bool, scale: float, k_start=None, k_end=None,
-           dq=None, dk=None, dv=None, workspace=None, stream=None, key_mask=None):
+           dq=None, dk=None, dv=None, workspace=None, stream=None, key_mask=None,
+           dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
     """dQ, dK, dV by recomputation via the library's fa_bwd (fa_bwd_masked
-    when key_mask is given; it must be the forward's).  Returns (dq, dk, dv)."""
+    when key_mask is given, fa_bwd_dropout when dropout_p > 0; mask and
+    dropout arguments must be the forward's).  Returns (dq, dk, dv)."""
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _need(t, n, torch.bfloat16, 4)
@@ -194,7 +211,14 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool, scale: float, k_start=None, k_en
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     bits = _mask_bits(key_mask, B, Sk, stream)
-    if bits is None:
+    if dropout_p > 0.0:
+        st = lib.fa_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d,
+                                int(bool(causal)), float(scale), _ptr(k_start), _ptr(k_end),
+                                _ptr(bits), float(dropout_p), int(seed), int(offset),
+                                _ptr(workspace), workspace.numel(), _stream(stream))
+        _check(st, "fa_bwd_dropout")
+    elif bits is None:
         st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d, int(bool(causal)),
                         float(scale), _ptr(k_start), _ptr(k_end), _ptr(workspace),

@@ -2,7 +2,9 @@
 // argument validation, TMA tensor-map encoding, workspace carving and kernel
 // launch.  No device memory is allocated here; no device memory is read on the
 // host (the calls stay asynchronous and capturable).
+#include <cfloat>
 #include <cmath>
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -123,6 +125,15 @@ fa_status make_map_acc(CUtensorMap* map, void* base, long heads, long rows, int 
   return FA_OK;
 }
 
+// Base-2 scale c = scale * log2(e) the kernels multiply scores by.  It is
+// kept >= 2^-126 so that a masked score (-inf) still gives -inf * c = -inf
+// (weight 0) when the caller's scale is 0; finite scores then give s * c far
+// below fp32 resolution, i.e. the exactly uniform weights of scale 0.
+float scale_log2_of(float scale) {
+  const float c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  return std::max(c, FLT_MIN);
+}
+
 fa_status check_sizes(int B, int Hq, int Hkv, int Sq, int Sk, int d) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1)
     return fail(FA_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d Hq=%d Hkv=%d Sq=%d Sk=%d)", B, Hq,
@@ -192,16 +203,37 @@ fa_status check_key_bits(const uint32_t* bits) {
   return FA_OK;
 }
 
+// Dropout arguments from the caller's probability, seed and offset: keep a
+// weight iff its Philox word is >= floor(p * 2^32) (computed in double, the
+// same integer threshold the reference computation uses).
+fa_status make_dropout(float p_drop, unsigned long long seed, unsigned int offset,
+                       fa::DropoutArgs* out) {
+  if (!(p_drop >= 0.f && p_drop < 1.f))
+    return fail(FA_ERR_INVALID_ARG, "dropout_p (%g) must lie in [0, 1)", (double)p_drop);
+  fa::DropoutArgs dr{};
+  dr.thr = static_cast<uint32_t>(std::floor(static_cast<double>(p_drop) * 4294967296.0));
+  dr.seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
+  dr.seed_hi = static_cast<uint32_t>(seed >> 32);
+  dr.offset = offset;
+  dr.scale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop)));
+  *out = dr;
+  return FA_OK;
+}
+
+const fa::DropoutArgs kNoDropout{0u, 0u, 0u, 0u, 1.f};
+
 fa_status fwd_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
-                     const SeqLayout& lay, const uint32_t* key_bits, cudaStream_t stream) {
+                     const SeqLayout& lay, const uint32_t* key_bits, const fa::DropoutArgs& drop,
+                     cudaStream_t stream) {
   FA_TRY(check_ptr(q, "q"));
   FA_TRY(check_ptr(k, "k"));
   FA_TRY(check_ptr(v, "v"));
   FA_TRY(check_ptr(o, "o"));
   FA_TRY(check_ptr(lse, "lse", true));
   FA_TRY(check_key_bits(key_bits));
-  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale is not finite");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(FA_ERR_INVALID_ARG, "scale (%g) must be finite and >= 0", (double)scale);
   FA_TRY(check_device());
 
   CUtensorMap tq, tk, tv;
@@ -218,6 +250,7 @@ fa_status fwd_launch(const void* q, const void* k, const void* v, void* o, float
   p.cu_k = lay.cu_k;
   p.key_bits = key_bits;
   p.mask_words = static_cast<int>(fa_key_mask_words(Sk));
+  p.drop = drop;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -235,7 +268,7 @@ fa_status fwd_launch(const void* q, const void* k, const void* v, void* o, float
   }
   p.causal = causal ? 1 : 0;
   p.scale = scale;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.scale_log2 = scale_log2_of(scale);
   p.rescale_log2 = 8.0f;
   if (1LL * p.n_rbu * p.units_per_rbu >= (1LL << 31))
     return fail(FA_ERR_INVALID_ARG, "grid too large");
@@ -247,8 +280,8 @@ fa_status fwd_launch(const void* q, const void* k, const void* v, void* o, float
 fa_status bwd_launch(const void* q, const void* k, const void* v, const void* o, const void* dout,
                      const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
                      int Sq, int Sk, int d, int causal, float scale, const SeqLayout& lay,
-                     const uint32_t* key_bits, void* workspace, size_t workspace_bytes,
-                     cudaStream_t stream) {
+                     const uint32_t* key_bits, const fa::DropoutArgs& drop, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
   FA_TRY(check_ptr(q, "q"));
   FA_TRY(check_ptr(k, "k"));
   FA_TRY(check_ptr(v, "v"));
@@ -259,7 +292,8 @@ fa_status bwd_launch(const void* q, const void* k, const void* v, const void* o,
   FA_TRY(check_ptr(dk, "dk"));
   FA_TRY(check_ptr(dv, "dv"));
   FA_TRY(check_key_bits(key_bits));
-  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale is not finite");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(FA_ERR_INVALID_ARG, "scale (%g) must be finite and >= 0", (double)scale);
   const size_t need = fa_bwd_workspace_size(B, Hq, Sq, d);
   if (!workspace || workspace_bytes < need)
     return fail(FA_ERR_WORKSPACE, "backward workspace needs %zu bytes, got %zu", need,
@@ -293,6 +327,7 @@ fa_status bwd_launch(const void* q, const void* k, const void* v, const void* o,
   p.cu_k = lay.cu_k;
   p.key_bits = key_bits;
   p.mask_words = static_cast<int>(fa_key_mask_words(Sk));
+  p.drop = drop;
   p.grid_b = lay.grid_b;
   p.n_kt = (lay.longest_k + fa::kTileN - 1) / fa::kTileN;
   p.B = B;
@@ -303,7 +338,7 @@ fa_status bwd_launch(const void* q, const void* k, const void* v, const void* o,
   p.group = Hq / Hkv;
   p.causal = causal ? 1 : 0;
   p.scale = scale;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.scale_log2 = scale_log2_of(scale);
   if (1LL * p.n_kt * p.grid_b * Hkv >= (1LL << 31))
     return fail(FA_ERR_INVALID_ARG, "grid too large");
   CUtensorMap tdq;
@@ -338,7 +373,27 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
   lay.k_start = k_start;
   lay.k_end = k_end;
   return fwd_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, lay, key_mask_bits,
-                    stream);
+                    kNoDropout, stream);
+}
+
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                         const int32_t* k_start, const int32_t* k_end,
+                         const uint32_t* key_mask_bits, float dropout_p,
+                         unsigned long long seed, unsigned int offset, cudaStream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, Sq, Sk, d));
+  FA_TRY(check_i32(k_start, "k_start"));
+  FA_TRY(check_i32(k_end, "k_end"));
+  fa::DropoutArgs dr{};
+  FA_TRY(make_dropout(dropout_p, seed, offset, &dr));
+  SeqLayout lay{};
+  lay.grid_b = B;
+  lay.longest_q = Sq;
+  lay.longest_k = Sk;
+  lay.k_start = k_start;
+  lay.k_end = k_end;
+  return fwd_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, lay, key_mask_bits,
+                    dr, stream);
 }
 
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -351,7 +406,7 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   FA_TRY(varlen_layout(cu_seqlens_q, cu_seqlens_k, nseq, max_seqlen_q, max_seqlen_k, total_q,
                        total_k, &lay));
   return fwd_launch(q, k, v, o, lse, 1, Hq, Hkv, total_q, total_k, d, causal, scale, lay,
-                    key_mask_bits, stream);
+                    key_mask_bits, kNoDropout, stream);
 }
 
 size_t fa_decode_workspace_size(int B, int Hq, int Sk_max, int d) {
@@ -373,7 +428,8 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
   FA_TRY(check_ptr(lse, "lse", true));
   if (!seqlens_k) return fail(FA_ERR_INVALID_ARG, "seqlens_k is NULL");
   FA_TRY(check_i32(seqlens_k, "seqlens_k"));
-  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale is not finite");
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(FA_ERR_INVALID_ARG, "scale (%g) must be finite and >= 0", (double)scale);
   const size_t need = fa_decode_workspace_size(B, Hq, Sk_max, d);
   if (!workspace || workspace_bytes < need)
     return fail(FA_ERR_WORKSPACE, "decode workspace needs %zu bytes, got %zu", need,
@@ -398,7 +454,7 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
   p.part_o = static_cast<float*>(workspace);
   p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                         align256(rows * d * sizeof(float)));
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.scale_log2 = scale_log2_of(scale);
   if (p.n_split > 65535 * 64 || 1LL * B > 65535)
     return fail(FA_ERR_INVALID_ARG, "decode grid too large");
   cudaError_t e = fa::launch_decode(d, p, stream);
@@ -437,7 +493,29 @@ fa_status fa_bwd_masked(const void* q, const void* k, const void* v, const void*
   lay.k_start = k_start;
   lay.k_end = k_end;
   return bwd_launch(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale, lay,
-                    key_mask_bits, workspace, workspace_bytes, stream);
+                    key_mask_bits, kNoDropout, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                         const int32_t* k_start, const int32_t* k_end,
+                         const uint32_t* key_mask_bits, float dropout_p,
+                         unsigned long long seed, unsigned int offset, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, Sq, Sk, d));
+  FA_TRY(check_i32(k_start, "k_start"));
+  FA_TRY(check_i32(k_end, "k_end"));
+  fa::DropoutArgs dr{};
+  FA_TRY(make_dropout(dropout_p, seed, offset, &dr));
+  SeqLayout lay{};
+  lay.grid_b = B;
+  lay.longest_q = Sq;
+  lay.longest_k = Sk;
+  lay.k_start = k_start;
+  lay.k_end = k_end;
+  return bwd_launch(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale, lay,
+                    key_mask_bits, dr, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
@@ -451,7 +529,7 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
   FA_TRY(varlen_layout(cu_seqlens_q, cu_seqlens_k, nseq, max_seqlen_q, max_seqlen_k, total_q,
                        total_k, &lay));
   return bwd_launch(q, k, v, o, dout, lse, dq, dk, dv, 1, Hq, Hkv, total_q, total_k, d, causal,
-                    scale, lay, key_mask_bits, workspace, workspace_bytes, stream);
+                    scale, lay, key_mask_bits, kNoDropout, workspace, workspace_bytes, stream);
 }
 
 size_t fa_key_mask_words(int Sk) {

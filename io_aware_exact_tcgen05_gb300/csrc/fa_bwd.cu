@@ -40,6 +40,7 @@
 #include <math.h>
 
 #include "fa_internal.h"
+#include "fa_philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(256) fa_bwd_convert(const BwdParams p, long lo
 }
 
 // ------------------------------------------------------------------ main --
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -337,6 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float c = p.scale_log2;
     const uint32_t ds_base = smem_u32(s.ds[0]);
+    // dropout: the four lanes of keys 4a..4a+3 share a Philox counter per
+    // query (the key tile starts on a multiple of 4 keys); lane (l & 3) of the
+    // group draws query t = l & 3 of each block of 4 and ballots hand every
+    // lane its own key's bits
+    const uint32_t grp4 = static_cast<uint32_t>(lane & ~3);
+    const uint32_t key4 = static_cast<uint32_t>(key) >> 2;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int g = it / n_qt;
@@ -373,10 +380,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(&s.s_full, it & 1, abort_flag, kSiteS)) { ok = false; break; }
       tc_fence_after();
       uint32_t pk[32];  // this half's P^T, bf16 pairs
+      uint32_t keepw[2] = {~0u, ~0u};  // dropout: bit q = query hf*64 + 32 cc + q kept
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t sr[32];
         tmem_ld32(t_S + lane_off + hf * 64 + cc * 32, sr);
+        if (DROP) {
+          const uint32_t bh = static_cast<uint32_t>(bz * p.Hq + h);
+          uint32_t kw = 0;
+#pragma unroll
+          for (int g4 = 0; g4 < 8; ++g4) {
+            const uint32_t qi = static_cast<uint32_t>(q0 + hf * 64 + cc * 32 + g4 * 4) +
+                                static_cast<uint32_t>(lane & 3);
+            const uint32_t k4 = dropout_keep4(p.drop, key4, qi, bh);
+            const uint32_t b0 = __ballot_sync(0xffffffffu, k4 & 1u);
+            const uint32_t b1 = __ballot_sync(0xffffffffu, k4 & 2u);
+            const uint32_t b2 = __ballot_sync(0xffffffffu, k4 & 4u);
+            const uint32_t b3 = __ballot_sync(0xffffffffu, k4 & 8u);
+            const uint32_t sel = (lane & 2) ? ((lane & 1) ? b3 : b2) : ((lane & 1) ? b1 : b0);
+            kw |= ((sel >> grp4) & 0xFu) << (4 * g4);
+          }
+          keepw[cc] = kw;
+        }
         tmem_wait_ld();
         uint32_t pw[16];
 #pragma unroll
@@ -392,8 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!key_in || q0 + qa < qmin) p0 = 0.f;
             if (!key_in || q0 + qa + 1 < qmin) p1 = 0.f;
           }
-          pw[e] = pack_bf16x2(p0, p1);
-          pk[cc * 16 + e] = pw[e];
+          pk[cc * 16 + e] = pack_bf16x2(p0, p1);
+          pw[e] = pk[cc * 16 + e];
+          if (DROP) {
+            const uint32_t kb = keepw[cc] >> (2 * e);
+            pw[e] &= ((kb & 1u) ? 0x0000ffffu : 0u) | ((kb & 2u) ? 0xffff0000u : 0u);
+          }
         }
         // P columns [64 hf + 16 cc, +16) hold scores this warp already loaded
         tmem_st16(t_S + lane_off + hf * 64 + cc * 16, pw);
@@ -415,9 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int qa = hf * 64 + cc * 32 + 2 * e;
-          const uint64_t dp2 =
-              f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
-                     nd2[qa >> 1]);
+          uint64_t dp2;
+          if (DROP) {  // dP of the dropped weights: keep / (1 - p) * <dO, v>
+            const uint32_t kb = keepw[cc] >> (2 * e);
+            dp2 = f2_fma(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
+                         f2_pack((kb & 1u) ? p.drop.scale : 0.f, (kb & 2u) ? p.drop.scale : 0.f),
+                         nd2[qa >> 1]);
+          } else {
+            dp2 = f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
+                         nd2[qa >> 1]);
+          }
           float d0, d1;
           f2_unpack(f2_mul(bf16x2_to_f2(pk[cc * 16 + e]), dp2), d0, d1);
           dw[e] = pack_bf16x2(d0, d1);
@@ -450,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
         const uint32_t src = (pass == 0) ? t_dK : t_dV;
-        const float mul = (pass == 0) ? p.scale : 1.f;
+        const float mul = (pass == 0) ? p.scale : (DROP ? p.drop.scale : 1.f);
         __nv_bfloat16* dst = (pass == 0) ? dkrow : dvrow;
 #pragma unroll
         for (int c2i = 0; c2i < D / 64; ++c2i) {
@@ -540,13 +576,14 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          cudaStream_t stream) {
   constexpr size_t smem = sizeof(BwdSmem<D>);
   static_assert(smem <= 232448, "backward shared memory exceeds the per-CTA limit");
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main<D>,
+  static bool configured[2] = {false, false};
+  const bool drop = p.drop.thr != 0;
+  if (!configured[drop]) {
+    cudaError_t e = cudaFuncSetAttribute(drop ? fa_bwd_main<D, true> : fa_bwd_main<D, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[drop] = true;
   }
   const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
   const long long pre_threads = rows * (D / 8);
@@ -556,7 +593,10 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const unsigned int grid = static_cast<unsigned int>(p.n_kt) * p.grid_b * p.Hkv;
   if (grid > 0) {  // packed sequences that all lack keys: dQ stays zero
     hook_before(stream);
-    fa_bwd_main<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, p);
+    if (drop)
+      fa_bwd_main<D, true><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, p);
+    else
+      fa_bwd_main<D, false><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, p);
     hook_after(stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -266,9 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float m_new = fmaxf(m, mx);
-      const bool grow = (m_new - m) * c > 0.f;  // NaN (both -inf) -> false
+      // the first finite max is always taken (also when c = 0); before it
+      // nothing is accumulated, so its rescale factor is 0
+      const bool first = (m == neg_inf()) && (m_new != neg_inf());
+      const bool grow = first || (m_new - m) * c > 0.f;  // NaN (both -inf) -> false
       if (__any_sync(0xffffffffu, grow)) {
-        const float alpha = grow ? ex2_approx((m - m_new) * c) : 1.f;
+        const float alpha = first ? 0.f : (grow ? ex2_approx((m - m_new) * c) : 1.f);
         l *= alpha;
         if (grow) m = m_new;
 #pragma unroll

@@ -31,6 +31,7 @@
 #include <math.h>
 
 #include "fa_internal.h"
+#include "fa_philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -100,11 +101,17 @@ __device__ __forceinline__ void mask_key_bits(uint32_t (&sr)[kTileN], uint4 kb) 
 // Weights 2^(s*c - mc) of the 64 scores sr[64*HALF, +64) (nmc2 holds -mc
 // twice), rounded to bf16 pairs and stored to TMEM columns [32*HALF, +32)
 // from t_p.  sum2 gathers the fp32 weights (for l); sr_lo/sr_hi gather the
-// rounded ones the PV MMA multiplies (for lr).
-template <int HALF>
+// rounded ones (for lr).  With DROP, the stored words of dropped weights are
+// cleared after the sums (l, lr and the LSE stay those of the undropped
+// softmax); key4 is the tile's first key / 4, row and bh the Philox counter's
+// query row and query head.
+template <int HALF, bool DROP>
 __device__ __forceinline__ void softmax_half(const uint32_t (&sr)[kTileN], uint64_t c2,
                                              uint64_t nmc2, uint32_t t_p, uint64_t (&sum2)[4],
-                                             float (&sr_lo)[4], float (&sr_hi)[4]) {
+                                             float (&sr_lo)[4], float (&sr_hi)[4],
+                                             const DropoutArgs& drop, uint32_t key4, uint32_t row,
+                                             uint32_t bh) {
+  uint32_t keep4 = 0;
   uint32_t pk[kTileN / 4];
 #pragma unroll
   for (int jq = 0; jq < kTileN / 4; ++jq) {
@@ -118,6 +125,11 @@ __device__ __forceinline__ void softmax_half(const uint32_t (&sr)[kTileN], uint6
     pk[jq] = pack_bf16x2(p0, p1);
     sum2[jq & 3] = f2_add(sum2[jq & 3], f2_pack(p0, p1));
     add_bf16x2_f32(sr_lo[jq & 3], sr_hi[jq & 3], pk[jq]);
+    if (DROP) {
+      if ((jq & 1) == 0) keep4 = dropout_keep4(drop, key4 + HALF * 16 + jq / 2, row, bh);
+      const uint32_t kb = keep4 >> (2 * (jq & 1));
+      pk[jq] &= ((kb & 1u) ? 0x0000ffffu : 0u) | ((kb & 2u) ? 0xffff0000u : 0u);
+    }
   }
   tmem_st32(t_p + HALF * 32, pk);
 }
@@ -128,11 +140,16 @@ __device__ __forceinline__ float sum_f2x4(const uint64_t (&v)[4]) {
   return a + b;
 }
 
-template <int D>
+// Kernel modes: the plain path carries no mask or dropout code at all.
+enum : int { kModePlain = 0, kModeKeyBits = 1, kModeDropout = 2 };
+
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
   using Smem = FwdSmem<D>;
+  constexpr bool DROP = MODE == kModeDropout;
+  constexpr bool BITS = MODE != kModePlain;  // key visibility bits may be present
   constexpr int NB = Smem::NB;
   constexpr int NS = Smem::NS;
   constexpr uint32_t kBoxBytes = Smem::kBox * 2;
@@ -336,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_s = tmem + t * kTileN + lane_off;
     const uint32_t t_o = tmem + 2 * kTileN + t * D + lane_off;
     const uint32_t t_p = t_s + kTileN / 2;  // P: bf16 pairs in S columns [64, 128)
+    const uint32_t bh = static_cast<uint32_t>(bz * p.Hq + h);  // dropout counter word 2
     const float c = p.scale_log2;
     // keys visible to this row: [klo, khi_row)
     int khi_row = kend;
@@ -354,13 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
         tmem_wait_ld();
         const int c0 = (j0 + j) * kTileN;
+        const uint32_t key4 = static_cast<uint32_t>(c0) >> 2;  // dropout counter word 0
         const bool need_mask = (c0 < klo) || (c0 + kTileN > khi_row);
         const bool masked_tile = __any_sync(0xffffffffu, need_mask);
         if (masked_tile) mask_scores<0, kTileN>(sr, c0, klo, khi_row);
         // key visibility bits of this tile (the same 128 bits for every row)
         uint4 kb = make_uint4(~0u, ~0u, ~0u, ~0u);
-        if (kbits) kb = __ldg(reinterpret_cast<const uint4*>(kbits + c0 / 32));
-        const bool bit_masked = (kb.x & kb.y & kb.z & kb.w) != ~0u;
+        if (BITS && kbits) kb = __ldg(reinterpret_cast<const uint4*>(kbits + c0 / 32));
+        const bool bit_masked = BITS && (kb.x & kb.y & kb.z & kb.w) != ~0u;
         if (bit_masked) mask_key_bits<0, kTileN>(sr, kb);
         // Fast path: weights relative to the running max as it stands.  The
         // max only keeps the weights finite, and the fp32 tile sum (needed for
@@ -375,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!exact) {
           const float mc = m * c;
           const uint64_t nmc2 = f2_pack(-mc, -mc);
-          softmax_half<0>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi);
-          softmax_half<1>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi);
+          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key4, i, bh);
+          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key4, i, bh);
           const float ts = sum_f2x4(sum2);
           exact = __any_sync(0xffffffffu, !(ts < kFastLimit));
           if (!exact) {
@@ -410,9 +429,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
                                  fmaxf(mx8[6], mx8[7]));
           const float m_new = fmaxf(m, mx);
-          // (m_new - m) is NaN only when both are -inf: no rescale then.
-          grow = (m_new - m) * c > p.rescale_log2;
-          alpha = grow ? ex2_approx((m - m_new) * c) : 1.f;  // 0 when m = -inf
+          // A row's first visible key always sets its max (also when c = 0,
+          // where (m_new - m) * c would be inf * 0); nothing is accumulated
+          // yet, so the rescale factor is 0.  Later the max moves only when it
+          // grows by more than the threshold.
+          const bool first = (m == neg_inf()) && (m_new != neg_inf());
+          grow = first || (m_new - m) * c > p.rescale_log2;
+          alpha = first ? 0.f : (grow ? ex2_approx((m - m_new) * c) : 1.f);
           if (grow) {
             l *= alpha;
             lr *= alpha;
@@ -426,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             sr_lo[q2] = 0.f;
             sr_hi[q2] = 0.f;
           }
-          softmax_half<0>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi);
-          softmax_half<1>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi);
+          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key4, i, bh);
+          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key4, i, bh);
           l += sum_f2x4(sum2);
           lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
                 ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
@@ -457,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- epilogue: O = u / l, LSE = m*scale + ln l ---------------------
     if (((t == 0) || active1) && ok && !warp_aborted(abort_flag)) {
       const bool live = l > 0.f;
-      const float inv = live ? 1.f / lr : 0.f;
+      const float inv = live ? (DROP ? p.drop.scale : 1.f) / lr : 0.f;
       const bool in_range = i < sq;
       const size_t row = (static_cast<size_t>(bz) * p.Hq + h) * p.Sq + qb + i;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
@@ -496,13 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdParams& p, cudaStream_t stream) {
+template <int D, int MODE>
+cudaError_t launch_fwd_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const FwdParams& p, cudaStream_t stream) {
   constexpr size_t smem = fwd_smem_bytes<D>();
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -510,9 +533,17 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   }
   const unsigned int grid = static_cast<unsigned int>(p.n_rbu) * p.units_per_rbu;
   hook_before(stream);
-  fa_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  fa_fwd_kernel<D, MODE><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   hook_after(stream);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, cudaStream_t stream) {
+  if (p.drop.thr != 0) return launch_fwd_dd<D, kModeDropout>(tq, tk, tv, p, stream);
+  if (p.key_bits) return launch_fwd_dd<D, kModeKeyBits>(tq, tk, tv, p, stream);
+  return launch_fwd_dd<D, kModePlain>(tq, tk, tv, p, stream);
 }
 
 }  // namespace

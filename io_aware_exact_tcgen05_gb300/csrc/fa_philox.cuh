@@ -1,0 +1,48 @@
+// fa_philox.cuh -- the counter-based generator behind attention dropout.
+//
+// Philox4x32-10 as published by Salmon, Moraes, Dror and Shaw ("Parallel
+// random numbers: as easy as 1, 2, 3", SC 2011): a 128-bit counter and a
+// 64-bit key go through ten rounds; each round multiplies two of the four
+// counter words by the paper's two 32-bit multipliers, swaps in the products'
+// high halves XORed with the other two words and the key, and the key is
+// advanced by the paper's two Weyl increments before every round but the
+// first.
+//
+// Dropout mapping (part of the forward/backward contract, FlashAttention_01
+// page, "why the backward can recompute" and "interface and implementation
+// constraints"): weight (query row i, key j) of query head bh = b * Hq + h
+// is kept iff word (j mod 4) of Philox4x32-10 at counter
+// (j / 4, i, bh, offset) under key (seed low, seed high) is >= floor(p * 2^32).
+#pragma once
+
+#include <cstdint>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+  constexpr uint32_t kWeyl0 = 0x9E3779B9u, kWeyl1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += kWeyl0;
+      k1 += kWeyl1;
+    }
+    const uint32_t hi_a = __umulhi(kMulA, c.x), lo_a = kMulA * c.x;
+    const uint32_t hi_b = __umulhi(kMulB, c.z), lo_b = kMulB * c.z;
+    c = make_uint4(hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a);
+  }
+  return c;
+}
+
+// Keep bits of keys 4*j4 .. 4*j4+3 at query row i of head bh (bit t = key 4*j4+t).
+__device__ __forceinline__ uint32_t dropout_keep4(const DropoutArgs& d, uint32_t j4, uint32_t i,
+                                                  uint32_t bh) {
+  const uint4 w = philox4x32_10(make_uint4(j4, i, bh, d.offset), d.seed_lo, d.seed_hi);
+  return (w.x >= d.thr ? 1u : 0u) | (w.y >= d.thr ? 2u : 0u) | (w.z >= d.thr ? 4u : 0u) |
+         (w.w >= d.thr ? 8u : 0u);
+}
+
+}  // namespace fa

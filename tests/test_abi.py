@@ -58,6 +58,7 @@ def test_fwd_validation_before_any_device_call(lib):
     assert _fwd(lib, o=18) == fa.FA_ERR_INVALID_ARG  # misaligned
     assert _fwd(lib, lse=8) == fa.FA_ERR_INVALID_ARG
     assert _fwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=-0.5) == fa.FA_ERR_INVALID_ARG
     assert b"16-byte" in lib.fa_last_error_detail() or True
 
 
@@ -149,3 +150,17 @@ def test_key_mask_words(lib):
     assert fa.fa_key_mask_words(129) == 8
     assert fa.fa_key_mask_words(8192) == 256
     assert fa.fa_key_mask_words(0) == 0
+
+
+def test_dropout_validation_before_any_device_call(lib):
+    def fwd(p):
+        return lib.fa_fwd_dropout(P(16), P(16), P(16), P(16), None, 1, 2, 2, 8, 8, 128, 0,
+                                  ctypes.c_float(0.1), None, None, None, ctypes.c_float(p), 1, 0,
+                                  None)
+    assert fwd(-0.1) == fa.FA_ERR_INVALID_ARG
+    assert fwd(1.0) == fa.FA_ERR_INVALID_ARG
+    assert fwd(float("nan")) == fa.FA_ERR_INVALID_ARG
+    st = lib.fa_bwd_dropout(P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16),
+                            1, 2, 2, 8, 8, 128, 1, ctypes.c_float(0.1), None, None, None,
+                            ctypes.c_float(1.5), 1, 0, P(256), 1 << 20, None)
+    assert st == fa.FA_ERR_INVALID_ARG

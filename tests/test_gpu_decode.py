@@ -14,9 +14,9 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run(B, Hq, Hkv, Smax, d, lens, seed=0, q_mult=1.0):
+def _run(B, Hq, Hkv, Smax, d, lens, seed=0, q_mult=1.0, scale=None):
     t = workloads.random_qkv(B, Hq, Hkv, 1, Smax, d, seed=seed, q_mult=q_mult)
-    scale = 1.0 / math.sqrt(d)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
     sl = torch.tensor(lens, dtype=torch.int32)
     o, lse = fa.fa_decode(t["q"].to(DEV), t["k"].to(DEV), t["v"].to(DEV), sl.to(DEV), scale)
     torch.cuda.synchronize()
@@ -52,3 +52,8 @@ def test_decode_empty_and_clamped_lengths():
 
 def test_decode_large_logits():
     _run(2, 8, 2, 3000, 128, [3000, 2999], seed=9, q_mult=8.0)
+
+
+def test_decode_zero_scale_gives_uniform_weights():
+    # the first finite max of a split is taken even when every score is 0
+    _run(3, 8, 2, 5000, 128, [5000, 1, 4097], seed=71, scale=0.0)

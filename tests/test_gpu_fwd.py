@@ -115,3 +115,13 @@ def test_score_jumps_after_first_tile(causal, Hq, Hkv, d):
 
 def test_many_tiles_random_scale():
     _run(2, 2, 2, 1100, 1100, 128, True, seed=13, scale=0.05)
+
+
+def test_zero_scale_gives_uniform_weights():
+    # scale 0: O is the mean of the visible V rows and LSE = ln(#visible),
+    # including the first tile of every row (no finite max from a score
+    # change) and rows whose first tiles are fully masked
+    B, H, S, d = 2, 2, 300, 128
+    ks = [0, 200]
+    _run(B, H, H, S, S, d, True, ks=ks, ke=[S, S], seed=61, scale=0.0)
+    _run(B, H, H, S, S, 64, False, seed=62, scale=0.0)
