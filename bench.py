@@ -399,6 +399,11 @@ def run_ours(args):
     e2e_ms = _sync_max(s2.elapsed_time(e2), ws) / args.steps
     e2e_value = job_tflops(f_fwd + f_bwd, e2e_ms, ws)
 
+    # ---- the widened rows (key masks, dropout, packed varlen), timed alone
+    nxt = None
+    if not args.skip_next:
+        nxt = next_rows_bench(fa, dev, peaks, w, q, k, v, do, kst, ken, o, lse, dq, dk, dv, wsb)
+
     # ---- decode (Sq = 1 over the ragged cache), timed alone
     dec = None
     if not args.skip_decode:
@@ -437,6 +442,7 @@ def run_ours(args):
                              "traffic": trafficf,
                              "algorithmic": f"{f_fwd:.4g} FLOP per launch"},
             "decode": dec,
+            "next_rows": nxt,
             "clocks": clocks.summary(),
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -449,6 +455,71 @@ def run_ours(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def next_rows_bench(fa, dev, peaks, w, q, k, v, do, kst, ken, o, lse, dq, dk, dv, wsb):
+    """The widened rows measured on the same shapes: a per-key boolean mask
+    (10% of keys hidden, seeded), dropout p = 0.1, and a packed varlen batch
+    (16 causal sequences, lengths uniform in [1024, 8192], seeded).  TFLOP/s
+    use the metric's formula on each problem's own sizes (masked keys and
+    dropped weights are not discounted)."""
+    peak_t = peaks["bf16_tflops"]
+
+    def timed(fn, reps=5):
+        for _ in range(2):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) / reps
+
+    out = {}
+    g = torch.Generator().manual_seed(1)
+    km = (torch.rand(w.B, w.Sk, generator=g) >= 0.1).to(dev)
+    bits = fa.fa_pack_key_mask(km)
+    f_f, f_b = w.flops_fwd(), w.flops_bwd()
+    ms_f = timed(lambda: fa.fa_fwd(q, k, v, True, w.scale, k_start=kst, k_end=ken, o=o, lse=lse,
+                                   key_mask=bits))
+    ms_b = timed(lambda: fa.fa_bwd(q, k, v, o, do, lse, True, w.scale, k_start=kst, k_end=ken,
+                                   dq=dq, dk=dk, dv=dv, workspace=wsb, key_mask=bits))
+    out["key_mask"] = {"workload": f"{WORKLOAD} + 10% of keys hidden by a boolean mask",
+                       "fwd_tflops": f_f / ms_f / 1e9, "fwd_frac": f_f / ms_f / 1e9 / peak_t,
+                       "bwd_tflops": f_b / ms_b / 1e9, "bwd_frac": f_b / ms_b / 1e9 / peak_t}
+    ms_f = timed(lambda: fa.fa_fwd(q, k, v, True, w.scale, k_start=kst, k_end=ken, o=o, lse=lse,
+                                   dropout_p=0.1, seed=1, offset=0))
+    ms_b = timed(lambda: fa.fa_bwd(q, k, v, o, do, lse, True, w.scale, k_start=kst, k_end=ken,
+                                   dq=dq, dk=dk, dv=dv, workspace=wsb, dropout_p=0.1, seed=1,
+                                   offset=0))
+    out["dropout"] = {"workload": f"{WORKLOAD} + dropout p = 0.1",
+                      "fwd_tflops": f_f / ms_f / 1e9, "fwd_frac": f_f / ms_f / 1e9 / peak_t,
+                      "bwd_tflops": f_b / ms_b / 1e9, "bwd_frac": f_b / ms_b / 1e9 / peak_t}
+    lens = torch.randint(1024, 8193, (16,), generator=g)
+    cu = torch.zeros(17, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0)
+    total, H, d = int(cu[-1]), w.Hq, w.d
+    gd = torch.Generator(device=dev).manual_seed(2)
+    vq, vk, vv, vdo = (torch.randn(H, total, d, generator=gd, device=dev).bfloat16()
+                       for _ in range(4))
+    cud = cu.to(dev)
+    L = int(lens.max())
+    vo, vl = fa.fa_fwd_varlen(vq, vk, vv, cud, cud, L, L, True, w.scale)
+    ws_v = torch.empty(fa.fa_bwd_workspace_size(1, H, total, d), dtype=torch.uint8, device=dev)
+    vgq, vgk, vgv = torch.empty_like(vq), torch.empty_like(vk), torch.empty_like(vv)
+    f_vf = sum(4.0 * H * int(n) * int(n) * d / 2 for n in lens)
+    ms_f = timed(lambda: fa.fa_fwd_varlen(vq, vk, vv, cud, cud, L, L, True, w.scale, o=vo, lse=vl))
+    ms_b = timed(lambda: fa.fa_bwd_varlen(vq, vk, vv, vo, vdo, vl, cud, cud, L, L, True, w.scale,
+                                          dq=vgq, dk=vgk, dv=vgv, workspace=ws_v))
+    out["varlen"] = {"workload": f"16 packed causal sequences, {total} tokens, H={H} d={d}",
+                     "fwd_tflops": f_vf / ms_f / 1e9, "fwd_frac": f_vf / ms_f / 1e9 / peak_t,
+                     "bwd_tflops": 2.5 * f_vf / ms_b / 1e9,
+                     "bwd_frac": 2.5 * f_vf / ms_b / 1e9 / peak_t}
+    st, word = fa.fa_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after the widened rows: {word:#x}")
+    return out
 
 
 def decode_bench(fa, dev, peaks, args, ws):
@@ -536,6 +607,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-next", action="store_true",
+                    help="skip the key-mask / dropout / varlen measurements")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--only", choices=["fwd", "bwd", "decode"], default=None)
     ap.add_argument("--decode-batch", type=int, default=0,
