@@ -325,3 +325,34 @@ def bwd_varlen(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: f
         dk[:, k0:k1] = b_[0]
         dv[:, k0:k1] = c[0]
     return dq, dk, dv
+
+
+def decode_e4m3(x) -> np.ndarray:
+    """Exact fp64 values of OCP FP8 E4M3 bytes ("Flash Attention" history page
+    2.2, FP8 in FA3): sign, 4 exponent bits (bias 7), 3 mantissa bits;
+    exponent 0 is subnormal (m/8 * 2^-6), the all-ones exponent with mantissa
+    7 is NaN, and there are no infinities (largest finite 448)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous().view(torch.uint8).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    b = np.asarray(x, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 15) & ((b & 7) == 7), np.nan, val)
+    return sign * val
+
+
+def fwd_fp8(q8, k8, vt8, causal: bool, scale: float, q_descale: float, k_descale: float,
+            v_descale: float, k_start=None, k_end=None):
+    """Forward of the dequantised FP8 problem: Q = q_descale * q8, K = k_descale
+    * k8, V = v_descale * vt8^T (vt8 is [B, Hkv, d, Sk]); the plain definition
+    of fwd on those exact values."""
+    q = decode_e4m3(q8) * q_descale
+    k = decode_e4m3(k8) * k_descale
+    v = np.ascontiguousarray(np.swapaxes(decode_e4m3(vt8), -1, -2)) * v_descale
+    return fwd(q, k, v, causal, scale, k_start=k_start, k_end=k_end)

@@ -397,6 +397,25 @@ def test_dropout_matches_explicit_mask_in_torch_fp64(causal):
     assert all(np.array_equal(x, y) for x, y in zip(a, b_))
 
 
+# --- FP8 (e4m3) inputs: the decoder is the format's definition ---
+
+def test_e4m3_decoder_known_codes_and_torch():
+    codes = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x3C: 1.5, 0x7E: 448.0, 0x80: -0.0, 0xC0: -2.0, 0xFE: -448.0}
+    got = orc.decode_e4m3(np.array(list(codes), dtype=np.uint8))
+    assert np.array_equal(got, np.array(list(codes.values())))
+    assert np.isnan(orc.decode_e4m3(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is None:
+        pytest.skip("torch without float8_e4m3fn")
+    allc = torch.arange(256, dtype=torch.uint8)
+    ref = allc.view(f8).to(torch.float64).numpy()
+    mine = orc.decode_e4m3(allc.numpy())
+    finite = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), ~finite)
+    assert np.array_equal(mine[finite], ref[finite])
+
+
 # --- chain-rule section: central differences on the 2x3x2 masked example ---
 
 def _loss(q, k, v):
