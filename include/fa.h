@@ -200,6 +200,24 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
                          unsigned long long seed, unsigned int offset, void* workspace,
                          size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * FP8 forward ("Flash Attention" history page 2.2: FA3 runs attention in
+ * FP8).  q [B,Hq,Sq,128], k [B,Hkv,Sk,128] and vt [B,Hkv,128,Sk] (V
+ * transposed: each head's value matrix stored head-dimension-major) hold
+ * e4m3 (OCP FP8 E4M3, bias 7, max 448) bytes; the attention is computed for
+ * Q = q_descale * q, K = k_descale * k, V = v_descale * v with the bf16
+ * forward's visibility rules (key interval, causal, GQA).  o (bf16
+ * [B,Hq,Sq,128]) and lse are written as by fa_fwd.  Both matrix products run
+ * in FP8 with fp32 accumulation; the softmax weights are rounded to e4m3 for
+ * the second product (O is normalised by the sum of the rounded weights, the
+ * LSE uses the exact fp32 sum).  d must be 128 (FA_ERR_UNSUPPORTED
+ * otherwise), Sk a multiple of 16, and the descale factors finite and > 0.
+ */
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                     float q_descale, float k_descale, float v_descale, const int32_t* k_start,
+                     const int32_t* k_end, cudaStream_t stream);
+
 /* Bytes of device workspace fa_decode needs for a cache of Sk_max positions:
    per (b, query head, split) partial outputs and logsumexps. */
 size_t fa_decode_workspace_size(int B, int Hq, int Sk_max, int d);

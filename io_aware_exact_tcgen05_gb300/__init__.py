@@ -27,7 +27,7 @@ FA_ERR_TIMEOUT = 5
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_decode", "fa_decode_workspace_size",
             "fa_decode_noalloc", "fa_fwd_masked", "fa_bwd_masked", "fa_fwd_varlen",
             "fa_bwd_varlen", "fa_fwd_dropout", "fa_bwd_dropout", "fa_key_mask_words",
-            "fa_pack_key_mask", "fa_device_status",
+            "fa_pack_key_mask", "fa_fwd_fp8", "fa_device_status",
             "fa_profile_next_launch", "fa_status_string", "fa_last_error_detail", "fa_version")
 
 _lib = None
@@ -64,6 +64,8 @@ def load_library(path: str = LIB_PATH):
                                    U64, U32, P, Z, P]
     lib.fa_fwd_dropout.restype = I
     lib.fa_bwd_dropout.restype = I
+    lib.fa_fwd_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, F, F, F, P, P, P]
+    lib.fa_fwd_fp8.restype = I
     lib.fa_key_mask_words.argtypes = [I]
     lib.fa_key_mask_words.restype = Z
     lib.fa_pack_key_mask.argtypes = [P, P, I, I, P]
@@ -185,6 +187,37 @@ def fa_fwd(q, k, v, causal: bool, scale: float, k_start=None, k_end=None, o=None
                                d, int(bool(causal)), float(scale), _ptr(k_start), _ptr(k_end),
                                _ptr(bits), _stream(stream))
         _check(st, "fa_fwd_masked")
+    return o, lse
+
+
+def _need8(t, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if t.dtype not in tuple(x for x in (f8, torch.uint8) if x is not None):
+        raise TypeError(f"{name} must hold e4m3 bytes (float8_e4m3fn or uint8), got {t.dtype}")
+    if not t.is_contiguous() or t.dim() != 4:
+        raise ValueError(f"{name} must be a contiguous 4-D tensor")
+
+
+def fa_fwd_fp8(q8, k8, vt8, causal: bool, scale: float, q_descale: float, k_descale: float,
+               v_descale: float, k_start=None, k_end=None, o=None, lse=None, stream=None):
+    """FP8 forward via fa_fwd_fp8: q8 [B,Hq,Sq,128], k8 [B,Hkv,Sk,128] and
+    vt8 [B,Hkv,128,Sk] (V transposed) e4m3 CUDA tensors with per-tensor
+    descale factors.  Returns (o bf16 [B,Hq,Sq,128], lse [B,Hq,Sq])."""
+    lib = load_library()
+    for t, n in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")):
+        _need8(t, n)
+    B, Hq, Sq, d = q8.shape
+    _, Hkv, Sk, _ = k8.shape
+    if tuple(vt8.shape) != (B, Hkv, d, Sk):
+        raise ValueError(f"vt8 must be [B, Hkv, d, Sk] = {(B, Hkv, d, Sk)}")
+    o = torch.empty(B, Hq, Sq, d, dtype=torch.bfloat16, device=q8.device) if o is None else o
+    lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q8.device) if lse is None else lse
+    st = lib.fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
+                        int(bool(causal)), float(scale), float(q_descale), float(k_descale),
+                        float(v_descale), _ptr(k_start), _ptr(k_end), _stream(stream))
+    _check(st, "fa_fwd_fp8")
     return o, lse
 
 

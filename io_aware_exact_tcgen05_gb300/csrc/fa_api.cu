@@ -106,6 +106,24 @@ fa_status make_map(CUtensorMap* map, const void* base, long heads, long rows, in
   return FA_OK;
 }
 
+// [heads, rows, cols] 8-bit tensor, 128-row x 128-column (128-byte) boxes,
+// 128-byte swizzle; out-of-range rows and columns read as zero.
+fa_status make_map_u8(CUtensorMap* map, const void* base, long heads, long rows, long cols) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols),
+                           static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (u8) failed (%d)", (int)r);
+  return FA_OK;
+}
+
 // [heads, rows, d] fp32 tensor (the backward's dQ accumulator), 32-row x
 // 32-column boxes (128 bytes wide), 128-byte swizzle; used as the target of
 // TMA reduce-add, which skips rows past the end of a head.
@@ -532,6 +550,59 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
                     scale, lay, key_mask_bits, kNoDropout, workspace, workspace_bytes, stream);
 }
 
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                     float q_descale, float k_descale, float v_descale, const int32_t* k_start,
+                     const int32_t* k_end, cudaStream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, Sq, Sk, d));
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8 supports d = 128 only (got %d)", d);
+  if (Sk % 16 != 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_fwd_fp8 needs Sk %% 16 == 0 (rows of V^T are Sk bytes)");
+  FA_TRY(check_ptr(q, "q"));
+  FA_TRY(check_ptr(k, "k"));
+  FA_TRY(check_ptr(vt, "vt"));
+  FA_TRY(check_ptr(o, "o"));
+  FA_TRY(check_ptr(lse, "lse", true));
+  FA_TRY(check_i32(k_start, "k_start"));
+  FA_TRY(check_i32(k_end, "k_end"));
+  if (!std::isfinite(scale) || scale < 0.f)
+    return fail(FA_ERR_INVALID_ARG, "scale (%g) must be finite and >= 0", (double)scale);
+  for (float ds : {q_descale, k_descale, v_descale})
+    if (!std::isfinite(ds) || !(ds > 0.f))
+      return fail(FA_ERR_INVALID_ARG, "descale factors must be finite and > 0");
+  FA_TRY(check_device());
+  CUtensorMap tq, tk, tvt;
+  FA_TRY(make_map_u8(&tq, q, 1L * B * Hq, Sq, d));
+  FA_TRY(make_map_u8(&tk, k, 1L * B * Hkv, Sk, d));
+  FA_TRY(make_map_u8(&tvt, vt, 1L * B * Hkv, d, Sk));  // [d rows, Sk columns] per head
+  fa::Fp8FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.k_start = k_start;
+  p.k_end = k_end;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.group = Hq / Hkv;
+  p.pack_heads = (p.group % 2 == 0) ? 1 : 0;
+  const int n_rb = (Sq + fa::kTileM - 1) / fa::kTileM;
+  p.n_rbu = p.pack_heads ? n_rb : (n_rb + 1) / 2;
+  p.units_per_rbu = p.pack_heads ? B * (Hq / 2) : B * Hq;
+  p.causal = causal ? 1 : 0;
+  const double qk = static_cast<double>(scale) * q_descale * k_descale;
+  p.scale_qk = static_cast<float>(qk);
+  p.scale_log2 = scale_log2_of(static_cast<float>(qk));
+  p.rescale_log2 = 8.0f;
+  p.v_descale = v_descale;
+  if (1LL * p.n_rbu * p.units_per_rbu >= (1LL << 31))
+    return fail(FA_ERR_INVALID_ARG, "grid too large");
+  cudaError_t e = fa::launch_fwd_fp8(tq, tk, tvt, p, stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "fa_fwd_fp8 launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 size_t fa_key_mask_words(int Sk) {
   if (Sk < 1) return 0;
   return static_cast<size_t>((Sk + fa::kTileN - 1) / fa::kTileN) * (fa::kTileN / 32);
@@ -556,7 +627,7 @@ fa_status fa_device_status(unsigned int* code_out, int clear) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
   const unsigned int w = fa::read_fwd_status(clear != 0) | fa::read_decode_status(clear != 0) |
-                         fa::read_bwd_status(clear != 0);
+                         fa::read_bwd_status(clear != 0) | fa::read_fwd_fp8_status(clear != 0);
   if (code_out) *code_out = w;
   if (w != 0) return fail(FA_ERR_TIMEOUT, "device status word 0x%08x", w);
   return ok();

@@ -1,0 +1,458 @@
+// fa_fwd_fp8.cu -- forward attention with FP8 (e4m3) inputs for sm_103a.
+//
+// The bf16 forward's schedule (two 128-row query slots per CTA, ping-ponged;
+// a TMA producer warp, an MMA warp and eight softmax warps) with 8-bit
+// operands on the tensor core ("Flash Attention" history page 2.2: FP8 in
+// FA3; both matrix products run in FP8, accumulation in fp32):
+//
+//   S_t = Q_t K_j^T     tcgen05.mma kind::f8f6f4, e4m3 A (Q) and B (K) from
+//                       shared memory, fp32 in TMEM; K = 32 per instruction
+//   P_t                 softmax warps: weights as in the bf16 forward, rounded
+//                       to e4m3 (saturating at 448) and written row by row to
+//                       shared memory in the MMA's K-major 128-byte-swizzled
+//                       layout
+//   O_t += P_t V_j      tcgen05.mma kind::f8f6f4, A = P (shared), B = V^T
+//                       (shared; V is passed transposed, [d, Sk] per head, so
+//                       that both operands of both products are K-major)
+//
+// Dequantisation is folded into the arithmetic: the score scale becomes
+// scale * q_descale * k_descale, and O is multiplied by v_descale once in the
+// epilogue.  Weights are kept below 448 (e4m3's largest finite value): the
+// fast path accepts a tile only while the row's fp32 weight sum stays below
+// it, and the exact path rescales once the max grows by more than 2^8.  O is
+// divided by the sum of the *rounded* weights (what the PV product used), l
+// (fp32, unrounded) gives the LSE.
+//
+// Method: as fa_fwd.cu ("Flash Attention" history page 1.2, 1.3, 2.1, 2.3;
+// FlashAttention_01 page, online-softmax derivation and masking rule).
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kD = 128;                   // head dimension (bytes per fp8 row)
+constexpr int kNS = 3;                    // K and V^T pipeline depth
+constexpr uint32_t kTile = 128 * 128;     // bytes of one 128 x 128 e4m3 tile
+constexpr float kFastLimitFp8 = 448.f;    // e4m3's largest finite value
+
+enum : unsigned int {
+  kSiteQ = 1, kSiteKFree, kSiteVFree, kSiteKFull, kSiteVFull, kSitePFull, kSiteSFull,
+  kSiteOFull, kSiteDrain
+};
+
+struct Fp8Smem {
+  uint8_t q[2][kTile];      // Q_t, rows = query rows, 128 bytes (= d) per row
+  uint8_t k[kNS][kTile];    // K_j, rows = keys
+  uint8_t vt[kNS][kTile];   // V_j^T, rows = head dimension, 128 keys per row
+  uint8_t p[2][kTile];      // P_t, rows = query rows, 128 keys per row
+  uint64_t bar_q;
+  uint64_t k_full[kNS], v_full[kNS];
+  uint64_t kv_free[kNS];    // round i read K tile i and V tile i - 1
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void mask_scores(uint32_t (&sr)[kTileN], int first, int count, int c0,
+                                            int klo, int khi) {
+#pragma unroll
+  for (int jj = 0; jj < kTileN; ++jj) {
+    if (jj < first || jj >= first + count) continue;
+    const int key = c0 + jj;
+    if (key < klo || key >= khi) sr[jj] = 0xff800000u;
+  }
+}
+
+// Weights 2^(s*c - mc) of the tile's 128 scores (nmc2 holds -mc twice),
+// rounded to e4m3 and written as the row's 128 bytes of P (eight swizzled
+// 16-byte chunks); sum2 gathers the fp32 weights (l), sr_lo/sr_hi the rounded
+// ones (lr).
+__device__ __forceinline__ void softmax_tile_fp8(const uint32_t (&sr)[kTileN], uint64_t c2,
+                                                 uint64_t nmc2, uint32_t p_row, int row,
+                                                 uint64_t (&sum2)[4], float (&sr_lo)[4],
+                                                 float (&sr_hi)[4]) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {  // 16 keys per chunk
+    uint32_t w[4];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {  // 4 keys per 32-bit word
+      uint16_t h[2];
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        const int jj = ch * 16 + q4 * 4 + pr * 2;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[jj]), __uint_as_float(sr[jj + 1])), c2, nmc2),
+                  x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        h[pr] = pack_e4m3x2(p0, p1);
+        const int a = (q4 * 2 + pr) & 3;
+        sum2[a] = f2_add(sum2[a], f2_pack(p0, p1));
+        add_e4m3x2_f32(sr_lo[a], sr_hi[a], h[pr]);
+      }
+      w[q4] = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
+    }
+    st_shared_v4(p_row + ((ch ^ (row & 7)) * 16), w[0], w[1], w[2], w[3]);
+  }
+}
+
+__device__ __forceinline__ float sum_f2x4(const uint64_t (&v)[4]) {
+  float a, b;
+  f2_unpack(f2_add(f2_add(v[0], v[1]), f2_add(v[2], v[3])), a, b);
+  return a + b;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tvt, const Fp8FwdParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  Fp8Smem& s = *reinterpret_cast<Fp8Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit (as the bf16 forward): heavy row blocks first -----------
+  const int L = blockIdx.x;
+  const int rbu = p.n_rbu - 1 - L / p.units_per_rbu;
+  const int u = L % p.units_per_rbu;
+  int b, h0, h1, r0, r1;
+  if (p.pack_heads) {
+    const int hpairs = p.Hq >> 1;
+    b = u / hpairs;
+    h0 = 2 * (u % hpairs);
+    h1 = h0 + 1;
+    r0 = r1 = rbu * kTileM;
+  } else {
+    b = u / p.Hq;
+    h0 = h1 = u % p.Hq;
+    r0 = rbu * 2 * kTileM;
+    r1 = r0 + kTileM;
+  }
+  const bool active1 = r1 < p.Sq;
+  const int hk = h0 / p.group;
+  int klo = p.k_start ? p.k_start[b] : 0;
+  int kend = p.k_end ? p.k_end[b] : p.Sk;
+  klo = max(0, min(klo, p.Sk));
+  kend = max(0, min(kend, p.Sk));
+  const int off = p.Sk - p.Sq;  // bottom-right causal alignment
+  int khi = kend;
+  if (p.causal) {
+    const int last_row = min((active1 ? r1 : r0) + kTileM - 1, p.Sq - 1);
+    khi = min(khi, last_row + off + 1);
+  }
+  int j0 = 0, n_tiles = 0;
+  if (khi > klo) {
+    j0 = klo / kTileN;
+    n_tiles = (khi + kTileN - 1) / kTileN - j0;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&s.bar_q, 1);
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.kv_free[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s.s_full[t], 1);
+      mbar_init(&s.p_full[t], 4);  // one arrival per softmax warp
+      mbar_init(&s.o_full[t], 1);
+    }
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  volatile int* abort_flag = &s.abort_flag;
+  if (warp == 8) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tvt);
+      const uint64_t keep = policy_evict_last();
+      mbar_arrive_expect_tx(&s.bar_q, (active1 ? 2 : 1) * kTile);
+      tma_load_3d(s.q[0], &tq, &s.bar_q, 0, r0, b * p.Hq + h0);
+      if (active1) tma_load_3d(s.q[1], &tq, &s.bar_q, 0, r1, b * p.Hq + h1);
+      const int zkv = b * p.Hkv + hk;
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % kNS;
+        const int use = j / kNS;
+        const int c0 = (j0 + j) * kTileN;
+        if (use > 0 && !mbar_wait(&s.kv_free[st], (use - 1) & 1, abort_flag, kSiteKFree)) break;
+        mbar_arrive_expect_tx(&s.k_full[st], kTile);
+        tma_load_3d_hint(s.k[st], &tk, &s.k_full[st], 0, c0, zkv, keep);
+        k_issued = j + 1;
+        if (use > 0) {
+          const int r = j - kNS + 1;
+          if (!mbar_wait(&s.kv_free[r % kNS], (r / kNS) & 1, abort_flag, kSiteVFree)) break;
+        }
+        // V^T tile: keys [c0, c0 + 128) of every head-dimension row
+        mbar_arrive_expect_tx(&s.v_full[st], kTile);
+        tma_load_3d_hint(s.vt[st], &tvt, &s.v_full[st], c0, 0, zkv, keep);
+        v_issued = j + 1;
+      }
+      if (*abort_flag) {
+        mbar_drain(&s.bar_q, 0, kSiteDrain);
+        for (int j = max(0, k_issued - kNS); j < k_issued; ++j)
+          mbar_drain(&s.k_full[j % kNS], (j / kNS) & 1, kSiteDrain);
+        for (int j = max(0, v_issued - kNS); j < v_issued; ++j)
+          mbar_drain(&s.v_full[j % kNS], (j / kNS) & 1, kSiteDrain);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------- MMA issuer --
+    if (n_tiles > 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kTileM, kTileN);  // N = keys or d, both 128
+      const int nslots = active1 ? 2 : 1;
+      const uint64_t qd0 = smem_desc_sw128(smem_u32(s.q[0]), 16, 1024);
+      const uint64_t qd1 = smem_desc_sw128(smem_u32(s.q[1]), 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(smem_u32(s.vt[0]), 16, 1024);
+      const uint64_t pd0 = smem_desc_sw128(smem_u32(s.p[0]), 16, 1024);
+      const uint64_t pd1 = smem_desc_sw128(smem_u32(s.p[1]), 16, 1024);
+      bool ok = mbar_wait_warp(&s.bar_q, 0, abort_flag, kSiteQ);
+      tc_fence_after();
+      for (int j = 0; ok && j <= n_tiles; ++j) {
+        if (j < n_tiles && !mbar_wait_warp(&s.k_full[j % kNS], (j / kNS) & 1, abort_flag, kSiteKFull))
+          break;
+        const uint64_t kd = desc_add(kd0, static_cast<uint32_t>(j % kNS) * kTile);
+        const uint64_t vd = desc_add(vd0, static_cast<uint32_t>((j + kNS - 1) % kNS) * kTile);
+        for (int t = 0; t < nslots; ++t) {
+          const uint32_t t_s = tmem + t * kTileN;
+          if (j > 0) {
+            // O_t += P_t(j-1) V_{j-1}: P from shared memory (generic-proxy
+            // stores fenced to the async proxy before p_full), V^T from TMA
+            if (!mbar_wait_warp(&s.p_full[t], (j - 1) & 1, abort_flag, kSitePFull)) {
+              ok = false;
+              break;
+            }
+            const int vs = (j - 1) % kNS;
+            if (t == 0 && !mbar_wait_warp(&s.v_full[vs], ((j - 1) / kNS) & 1, abort_flag, kSiteVFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();  // the softmax warps' TMEM reads of S_t come first
+            const uint32_t t_o = tmem + 2 * kTileN + t * kD;
+            const uint64_t pd = t ? pd1 : pd0;
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 32; ++kk)
+              mma_ss_warp_f8(t_o, desc_add(pd, kk * 32), desc_add(vd, kk * 32), idesc,
+                             (j > 1 || kk > 0) ? 1u : 0u);
+          }
+          if (j < n_tiles) {
+            const uint64_t qd = t ? qd1 : qd0;
+#pragma unroll
+            for (int kk = 0; kk < kD / 32; ++kk)
+              mma_ss_warp_f8(t_s, desc_add(qd, kk * 32), desc_add(kd, kk * 32), idesc,
+                             kk > 0 ? 1u : 0u);
+            mma_commit_warp(&s.s_full[t]);
+          } else {
+            mma_commit_warp(&s.o_full[t]);
+          }
+        }
+        if (!ok) break;
+        if (j < n_tiles) mma_commit_warp(&s.kv_free[j % kNS]);
+      }
+      if (warp_aborted(abort_flag)) {
+        mma_commit_warp(&s.drain);
+        mbar_drain(&s.drain, 0, kSiteDrain);
+      }
+    }
+  } else {
+    // ---------------------------------------------------- softmax warps --
+    const int t = warp >> 2;
+    const int row_in_tile = (warp & 3) * 32 + lane;
+    const int i = (t == 0 ? r0 : r1) + row_in_tile;
+    const int h = (t == 0) ? h0 : h1;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + t * kTileN + lane_off;
+    const uint32_t t_o = tmem + 2 * kTileN + t * kD + lane_off;
+    // this row's 128 bytes of P: 8-row swizzle atoms of 1024 bytes
+    const uint32_t p_row = smem_u32(s.p[t]) + static_cast<uint32_t>(row_in_tile) * 128;
+    const float c = p.scale_log2;
+    int khi_row = kend;
+    if (p.causal) khi_row = min(khi_row, i + off + 1);
+    float m = neg_inf();
+    float l = 0.f;   // fp32 weights
+    float lr = 0.f;  // e4m3-rounded weights
+    bool ok = (t == 0) || active1;
+    if (ok && n_tiles > 0) {
+      for (int j = 0; j < n_tiles; ++j) {
+        if (!mbar_wait_warp(&s.s_full[t], j & 1, abort_flag, kSiteSFull)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[kTileN];
+#pragma unroll
+        for (int cc = 0; cc < kTileN / 32; ++cc)
+          tmem_ld32(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+        tmem_wait_ld();
+        const int c0 = (j0 + j) * kTileN;
+        const bool need_mask = (c0 < klo) || (c0 + kTileN > khi_row);
+        if (__any_sync(0xffffffffu, need_mask)) mask_scores(sr, 0, kTileN, c0, klo, khi_row);
+        // fast path against the running max; exact path when a row has no
+        // max yet or a weight could exceed e4m3's range
+        bool exact = __any_sync(0xffffffffu, m == neg_inf());
+        const uint64_t c2 = f2_pack(c, c);
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+        float sr_lo[4] = {0.f, 0.f, 0.f, 0.f}, sr_hi[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!exact) {
+          const float mc = m * c;
+          softmax_tile_fp8(sr, c2, f2_pack(-mc, -mc), p_row, row_in_tile, sum2, sr_lo, sr_hi);
+          const float ts = sum_f2x4(sum2);
+          exact = __any_sync(0xffffffffu, !(ts < kFastLimitFp8));
+          if (!exact) {
+            l += ts;
+            lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
+                  ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
+          }
+        }
+        bool grow = false;
+        float alpha = 1.f;
+        if (exact) {
+          // the scores are still in registers (P went to shared memory)
+          float mx = neg_inf();
+#pragma unroll
+          for (int jj = 0; jj < kTileN; jj += 2)
+            mx = max3f(mx, __uint_as_float(sr[jj]), __uint_as_float(sr[jj + 1]));
+          const float m_new = fmaxf(m, mx);
+          const bool first = (m == neg_inf()) && (m_new != neg_inf());
+          grow = first || (m_new - m) * c > p.rescale_log2;
+          alpha = first ? 0.f : (grow ? ex2_approx((m - m_new) * c) : 1.f);
+          if (grow) {
+            l *= alpha;
+            lr *= alpha;
+            m = m_new;
+          }
+          const float mc = (m == neg_inf()) ? 0.f : m * c;
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2) {
+            sum2[q2] = 0ull;
+            sr_lo[q2] = 0.f;
+            sr_hi[q2] = 0.f;
+          }
+          softmax_tile_fp8(sr, c2, f2_pack(-mc, -mc), p_row, row_in_tile, sum2, sr_lo, sr_hi);
+          l += sum_f2x4(sum2);
+          lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
+                ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
+        }
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // O_t is quiescent: PV_t(j-1) completed before S_t(j) was signalled
+#pragma unroll
+          for (int cc = 0; cc < kD / 32; ++cc) {
+            uint32_t orr[32];
+            tmem_ld32(t_o + cc * 32, orr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q2 = 0; q2 < 32; ++q2)
+              orr[q2] = __float_as_uint(__uint_as_float(orr[q2]) * alpha);
+            tmem_st32(t_o + cc * 32, orr);
+          }
+          tmem_wait_st();
+        }
+        // P (generic stores) must be visible to the MMA's async-proxy reads;
+        // the S loads and any O rescale are ordered by the tcgen05 fence
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.p_full[t]);
+      }
+      if (ok) ok = mbar_wait_warp(&s.o_full[t], 0, abort_flag, kSiteOFull);
+      tc_fence_after();
+    }
+    // ---- epilogue: O = v_descale * u / lr, LSE = m * scale_qk + ln l -------
+    if (((t == 0) || active1) && ok && !warp_aborted(abort_flag)) {
+      const bool live = l > 0.f;
+      const float inv = live ? p.v_descale / lr : 0.f;
+      const bool in_range = i < p.Sq;
+      const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Sq + i;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * kD;
+#pragma unroll 1
+      for (int cc = 0; cc < kD / 32; ++cc) {
+        uint32_t orr[32];
+        if (n_tiles > 0) {
+          tmem_ld32(t_o + cc * 32, orr);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int q2 = 0; q2 < 32; ++q2) orr[q2] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int q2 = 0; q2 < 16; ++q2)
+          pk[q2] = pack_bf16x2(__uint_as_float(orr[2 * q2]) * inv,
+                               __uint_as_float(orr[2 * q2 + 1]) * inv);
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2)
+            dst[q2] = make_uint4(pk[4 * q2], pk[4 * q2 + 1], pk[4 * q2 + 2], pk[4 * q2 + 3]);
+        }
+      }
+      if (in_range && p.lse) p.lse[row] = live ? fmaf(m, p.scale_qk, logf(l)) : neg_inf();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                           const Fp8FwdParams& p, cudaStream_t stream) {
+  constexpr size_t smem = sizeof(Fp8Smem) + 1024;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_fp8_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned int grid = static_cast<unsigned int>(p.n_rbu) * p.units_per_rbu;
+  hook_before(stream);
+  fa_fwd_fp8_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tvt, p);
+  hook_after(stream);
+  return cudaGetLastError();
+}
+
+unsigned int read_fwd_fp8_status(bool clear) {
+  unsigned int v = 0;
+  cudaMemcpyFromSymbol(&v, g_status, sizeof v);
+  if (clear) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_status, &z, sizeof z);
+  }
+  return v;
+}
+
+}  // namespace fa

@@ -71,6 +71,29 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream);
 unsigned int read_fwd_status(bool clear);
 
+// FP8 (e4m3) forward: the batched layout, key interval, causal rule and GQA
+// of FwdParams; Q, K and V^T are e4m3 with per-tensor dequantisation factors.
+struct Fp8FwdParams {
+  void* o;             // bf16 [B,Hq,Sq,128]
+  float* lse;          // fp32 [B,Hq,Sq] or nullptr
+  const int32_t* k_start;
+  const int32_t* k_end;
+  int B, Hq, Hkv, Sq, Sk;
+  int group;
+  int pack_heads;
+  int n_rbu;
+  int units_per_rbu;
+  int causal;
+  float scale_qk;      // scale * q_descale * k_descale (natural log units)
+  float scale_log2;    // scale_qk * log2(e), kept >= 2^-126
+  float rescale_log2;
+  float v_descale;
+};
+
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                           const Fp8FwdParams& p, cudaStream_t stream);
+unsigned int read_fwd_fp8_status(bool clear);
+
 struct DecodeParams {
   const void* q;        // bf16 [B,Hq,1,d]
   const void* k;        // bf16 [B,Hkv,Sk_max,d]

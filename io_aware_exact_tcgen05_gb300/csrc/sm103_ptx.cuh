@@ -279,6 +279,18 @@ __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// kind::f8f6f4 form of mma_ss_warp (K = 32 per instruction for 8-bit inputs).
+__device__ __forceinline__ void mma_ss_warp_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -441,6 +453,31 @@ __device__ __forceinline__ void add_bf16x2_f32(float& acc_lo, float& acc_hi, uin
       "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
       : "+f"(acc_lo), "+f"(acc_hi)
       : "r"(w));
+}
+
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (type code 0),
+// fp32 accumulation, both operands K-major; same field layout as the f16 kind.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Two fp32 values -> two e4m3 bytes (round to nearest, saturating to +-448):
+// lo in the low byte, hi in the high byte.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// acc_lo += low e4m3 byte of w, acc_hi += high byte (exact widening through f16,
+// one fp32 rounding per add).
+__device__ __forceinline__ void add_e4m3x2_f32(float& acc_lo, float& acc_hi, uint16_t w) {
+  asm("{\n\t.reg .b32 h2;\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h2, %2;\n\t"
+      "mov.b32 {lo, hi}, h2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "h"(w));
 }
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {

@@ -164,3 +164,14 @@ def test_dropout_validation_before_any_device_call(lib):
                             1, 2, 2, 8, 8, 128, 1, ctypes.c_float(0.1), None, None, None,
                             ctypes.c_float(1.5), 1, 0, P(256), 1 << 20, None)
     assert st == fa.FA_ERR_INVALID_ARG
+
+
+def test_fp8_validation_before_any_device_call(lib):
+    def fwd8(d=128, Sk=128, qd=1.0):
+        return lib.fa_fwd_fp8(P(16), P(16), P(16), P(16), None, 1, 2, 2, 8, Sk, d, 0,
+                              ctypes.c_float(0.1), ctypes.c_float(qd), ctypes.c_float(1.0),
+                              ctypes.c_float(1.0), None, None, None)
+    assert fwd8(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert fwd8(Sk=100) == fa.FA_ERR_INVALID_ARG  # V^T rows must be whole 16-byte units
+    assert fwd8(qd=0.0) == fa.FA_ERR_INVALID_ARG
+    assert fwd8(qd=float("inf")) == fa.FA_ERR_INVALID_ARG

@@ -1,0 +1,91 @@
+"""GPU FP8 (e4m3) forward (fa_fwd_fp8 through the C ABI) against the FP64
+oracle run on the exactly dequantised inputs.
+
+Tolerance, derived from the arithmetic: the dequantised inputs are exact and
+fp32 accumulation of e4m3 products is exact to ~2^-24, so the error comes from
+rounding the softmax weights to e4m3 for the PV product.  A rounded weight
+has relative error <= 2^-4 (normal range) or absolute error <= 2^-10
+(subnormals and flush); the kernel's weights are relative to a running max,
+so the row's weight sum l >= 1, and O is normalised by the sum of the rounded
+weights.  Hence, per row i and output column c,
+  |O_gpu - O| <= (2^-4 / (1 - 2^-4)) * sum_j P_ij |v_jc - O_ic|
+               + (2^-10 / (1 - 2^-4)) * sum_j |v_jc - O_ic|
+plus the bf16 rounding of the output (bf16 keeps 8 significant bits: at
+most 2^-8 |O|); a 1e-4 floor absorbs fp32 accumulation.  The LSE comes from
+the exact fp32 weight sum: 1e-3 as always."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import io_aware_exact_tcgen05_gb300 as fa
+from io_aware_exact_tcgen05_gb300 import workloads
+from oracle import oracle as orc
+from tests.parity import check_lse, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+F8 = getattr(torch, "float8_e4m3fn", None)
+
+
+def _quant(x):
+    """e4m3 bytes of x / descale with descale = max|x| / 448 (per tensor)."""
+    xf = x.float()
+    ds = float(xf.abs().max()) / 448.0
+    return (xf / ds).to(F8), ds
+
+
+def _case(B, Hq, Hkv, Sq, Sk, causal, seed, ks=None, ke=None):
+    if F8 is None:
+        pytest.skip("torch without float8_e4m3fn")
+    d = 128
+    t = workloads.random_qkv(B, Hq, Hkv, Sq, Sk, d, seed=seed)
+    q8, qd = _quant(t["q"])
+    k8, kd = _quant(t["k"])
+    v8, vd = _quant(t["v"])
+    vt8 = v8.transpose(-1, -2).contiguous()
+    scale = 1.0 / math.sqrt(d)
+    kst = None if ks is None else torch.tensor(ks, dtype=torch.int32)
+    ken = None if ke is None else torch.tensor(ke, dtype=torch.int32)
+    o, lse = fa.fa_fwd_fp8(q8.to(DEV), k8.to(DEV), vt8.to(DEV), causal, scale, qd, kd, vd,
+                           k_start=None if kst is None else kst.to(DEV),
+                           k_end=None if ken is None else ken.to(DEV))
+    torch.cuda.synchronize()
+    st, word = fa.fa_device_status()
+    assert st == 0, hex(word)
+    ro, rl = orc.fwd_fp8(q8, k8, vt8, causal, scale, qd, kd, vd, k_start=kst, k_end=ken)
+    check_lse(to_np(lse), rl)
+    # the bound needs P and V of the dequantised problem
+    qx = orc.decode_e4m3(q8) * qd
+    kx = orc.decode_e4m3(k8) * kd
+    vx = np.swapaxes(orc.decode_e4m3(vt8), -1, -2) * vd
+    P = orc.probs(qx, kx, vx, causal, scale, k_start=kst, k_end=ken)  # [B,Hq,Sq,Sk]
+    rep = Hq // Hkv
+    A = np.zeros_like(ro)     # sum_j P_ij |v_jc - O_ic|
+    Bsum = np.zeros_like(ro)  # sum over visible j of |v_jc - O_ic|
+    for b in range(B):
+        for h in range(Hq):
+            vh = vx[b, h // rep]
+            for i0 in range(0, Sq, 64):
+                dv_ = np.abs(vh[None, :, :] - ro[b, h, i0:i0 + 64, None, :])  # [rows, Sk, d]
+                Pb = P[b, h, i0:i0 + 64]
+                A[b, h, i0:i0 + 64] = np.einsum("ij,ijc->ic", Pb, dv_)
+                Bsum[b, h, i0:i0 + 64] = np.einsum("ij,ijc->ic", (Pb > 0).astype(np.float64), dv_)
+    bound = (2.0 ** -4 * A + 2.0 ** -10 * Bsum) / (1 - 2.0 ** -4) + 2.0 ** -8 * np.abs(ro) + 1e-4
+    got = to_np(o)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ro)
+    worst = float((err / bound).max())
+    assert worst <= 1.0, f"O error exceeds the e4m3 weight-rounding bound by {worst:.3f}x"
+    return float(err.max()), float(np.sqrt((err ** 2).mean()))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_within_rounding_bound(causal):
+    _case(1, 4, 2, 384, 384, causal, seed=81)
+
+
+def test_fp8_forward_rectangular_interval_and_slots():
+    _case(2, 3, 3, 200, 512, False, seed=82, ks=[0, 100], ke=[512, 333])
+    _case(1, 2, 2, 130, 300 // 16 * 16, True, seed=83)
