@@ -459,8 +459,9 @@ def run_ours(args):
 
 def next_rows_bench(fa, dev, peaks, w, q, k, v, do, kst, ken, o, lse, dq, dk, dv, wsb):
     """The widened rows measured on the same shapes: a per-key boolean mask
-    (10% of keys hidden, seeded), dropout p = 0.1, and a packed varlen batch
-    (16 causal sequences, lengths uniform in [1024, 8192], seeded).  TFLOP/s
+    (10% of keys hidden, seeded), dropout p = 0.1, a packed varlen batch
+    (16 causal sequences, lengths uniform in [1024, 8192], seeded) and the
+    FP8 forward (per-tensor e4m3 quantisation of the same Q, K, V).  TFLOP/s
     use the metric's formula on each problem's own sizes (masked keys and
     dropped weights are not discounted)."""
     peak_t = peaks["bf16_tflops"]
@@ -516,6 +517,22 @@ def next_rows_bench(fa, dev, peaks, w, q, k, v, do, kst, ken, o, lse, dq, dk, dv
                      "fwd_tflops": f_vf / ms_f / 1e9, "fwd_frac": f_vf / ms_f / 1e9 / peak_t,
                      "bwd_tflops": 2.5 * f_vf / ms_b / 1e9,
                      "bwd_frac": 2.5 * f_vf / ms_b / 1e9 / peak_t}
+    # FP8 (e4m3) forward on the same shapes; per-tensor descale = max|x| / 448
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is not None:
+        def quant(x):
+            ds = float(x.float().abs().max()) / 448.0
+            return (x.float() / ds).to(f8), ds
+        q8, qd = quant(q)
+        k8, kd = quant(k)
+        v8, vd = quant(v)
+        vt8 = v8.transpose(-1, -2).contiguous()
+        peak8 = 2.0 * peak_t  # the nominal FP8 : BF16 dense ratio (4.5 : 2.25 PFLOP/s)
+        ms_f = timed(lambda: fa.fa_fwd_fp8(q8, k8, vt8, True, w.scale, qd, kd, vd, k_start=kst,
+                                           k_end=ken, o=o, lse=lse))
+        out["fp8_fwd"] = {"workload": f"{WORKLOAD}, Q/K/V in e4m3 (V transposed)",
+                          "fwd_tflops": f_f / ms_f / 1e9, "fwd_frac": f_f / ms_f / 1e9 / peak8,
+                          "peak": peak8, "peak_source": "2 x measured bf16 (nominal FP8:BF16)"}
     st, word = fa.fa_device_status()
     if st != 0:
         raise RuntimeError(f"device status after the widened rows: {word:#x}")
