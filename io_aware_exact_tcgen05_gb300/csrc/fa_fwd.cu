@@ -26,6 +26,15 @@
 // Warp roles (320 threads): warps 0-3 softmax of slot 0, warps 4-7 softmax of
 // slot 1 (a warp may only touch TMEM lanes 32*(warp%4) .. +31, which are the
 // rows it owns), warp 8 TMA producer, warp 9 MMA issuer and TMEM owner.
+//
+// The kernel is persistent: one CTA per SM walks a fixed sequence of work
+// units (the heavy-first list, taken in alternating directions block by
+// block so heavy and light units pair up).  Barrier phases run on across
+// units; the next unit's Q is loaded once the current unit's last S product
+// has read Q, its first S products overlap the current epilogue, and its
+// first PV into O waits only until the epilogue has read O.
+#include <algorithm>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -55,11 +64,15 @@ struct FwdSmem {
   __nv_bfloat16 k[NS][NB][kBox];
   __nv_bfloat16 v[NS][NB][kBox];
   uint64_t bar_q;
+  uint64_t q_free;             // the unit's last S product has read Q
   uint64_t k_full[NS], v_full[NS];
-  // kv_free[i % NS] completes a phase when every MMA of issue round i has
-  // finished: round i reads K tile i and V tile i - 1, so it frees K stage
-  // i % NS and V stage (i - 1) % NS (one commit per round instead of two).
+  // kv_free[g % NS] completes a phase when the round issuing S of tile g
+  // (g counts tiles across the CTA's units) has finished.  That round also
+  // finishes PV of tile g - 1, whether it belongs to the same unit or closes
+  // the previous one (a commit covers every earlier MMA), so it frees K
+  // stage g % NS and V stage (g - 1) % NS: one commit per tile.
   uint64_t kv_free[NS];
+  uint64_t o_empty[2];          // the slot's softmax warps have read O
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t drain;  // MMA teardown after an abort
   uint32_t tmem_base;
@@ -143,6 +156,67 @@ __device__ __forceinline__ float sum_f2x4(const uint64_t (&v)[4]) {
 // Kernel modes: the plain path carries no mask or dropout code at all.
 enum : int { kModePlain = 0, kModeKeyBits = 1, kModeDropout = 2 };
 
+// One work unit: two 128-row query tiles ("slots") and the key tiles they
+// see.  Units are numbered heavy (late) row blocks first; every role of a
+// CTA walks the same unit sequence, so their barrier phases stay in step.
+struct Unit {
+  int b, h0, h1, r0, r1;
+  int sq, qb, bz;        // logical rows [0, sq) from packed row qb of tensor batch bz
+  int klo, kend, off;    // visible key interval and bottom-right causal offset
+  int hk, j0, n_tiles;
+  bool rows, active1;    // rows: slot 0 has rows at all
+};
+
+__device__ __forceinline__ Unit unit_at(const FwdParams& p, int U) {
+  Unit u;
+  const int rbu = p.n_rbu - 1 - U / p.units_per_rbu;
+  const int w = U % p.units_per_rbu;
+  if (p.pack_heads) {
+    const int hpairs = p.Hq >> 1;
+    u.b = w / hpairs;
+    u.h0 = 2 * (w % hpairs);
+    u.h1 = u.h0 + 1;
+    u.r0 = u.r1 = rbu * kTileM;
+  } else {
+    u.b = w / p.Hq;
+    u.h0 = u.h1 = w % p.Hq;
+    u.r0 = rbu * 2 * kTileM;
+    u.r1 = u.r0 + kTileM;
+  }
+  u.sq = p.Sq;
+  u.qb = 0;
+  u.bz = u.b;
+  if (p.cu_q) {  // packed ragged: b is the sequence
+    u.qb = max(0, min(p.cu_q[u.b], p.Sq));
+    u.sq = max(0, min(p.cu_q[u.b + 1], p.Sq) - u.qb);
+    u.klo = max(0, min(p.cu_k[u.b], p.Sk));
+    u.kend = max(u.klo, min(p.cu_k[u.b + 1], p.Sk));
+    u.off = u.kend - u.sq;  // bottom-right causal alignment within the sequence
+    u.bz = 0;
+  } else {
+    u.klo = p.k_start ? p.k_start[u.b] : 0;
+    u.kend = p.k_end ? p.k_end[u.b] : p.Sk;
+    u.klo = max(0, min(u.klo, p.Sk));
+    u.kend = max(0, min(u.kend, p.Sk));
+    u.off = p.Sk - p.Sq;  // bottom-right causal alignment
+  }
+  u.rows = u.r0 < u.sq;
+  u.active1 = u.r1 < u.sq;
+  u.hk = u.h0 / p.group;
+  int khi = u.kend;
+  if (p.causal) {
+    const int last_row = min((u.active1 ? u.r1 : u.r0) + kTileM - 1, u.sq - 1);
+    khi = min(khi, last_row + u.off + 1);
+  }
+  u.j0 = 0;
+  u.n_tiles = 0;
+  if (u.rows && khi > u.klo) {
+    u.j0 = u.klo / kTileN;
+    u.n_tiles = (khi + kTileN - 1) / kTileN - u.j0;
+  }
+  return u;
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -158,58 +232,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work unit: heavy (late) row blocks are launched first -------------
-  const int L = blockIdx.x;
-  const int rbu = p.n_rbu - 1 - L / p.units_per_rbu;
-  const int u = L % p.units_per_rbu;
-  int b, h0, h1, r0, r1;
-  if (p.pack_heads) {
-    const int hpairs = p.Hq >> 1;
-    b = u / hpairs;
-    h0 = 2 * (u % hpairs);
-    h1 = h0 + 1;
-    r0 = r1 = rbu * kTileM;
-  } else {
-    b = u / p.Hq;
-    h0 = h1 = u % p.Hq;
-    r0 = rbu * 2 * kTileM;
-    r1 = r0 + kTileM;
-  }
-  // This unit's rows: logical rows [0, sq) start at packed row qb of tensor
-  // batch bz.  Keys [klo, kend) are in the K/V tensor's own row coordinates.
-  int sq = p.Sq, qb = 0, bz = b, klo, kend, off;
-  if (p.cu_q) {  // packed ragged: b is the sequence
-    qb = max(0, min(p.cu_q[b], p.Sq));
-    sq = max(0, min(p.cu_q[b + 1], p.Sq) - qb);
-    klo = max(0, min(p.cu_k[b], p.Sk));
-    kend = max(klo, min(p.cu_k[b + 1], p.Sk));
-    off = kend - sq;  // bottom-right causal alignment within the sequence
-    bz = 0;
-  } else {
-    klo = p.k_start ? p.k_start[b] : 0;
-    kend = p.k_end ? p.k_end[b] : p.Sk;
-    klo = max(0, min(klo, p.Sk));
-    kend = max(0, min(kend, p.Sk));
-    off = p.Sk - p.Sq;  // bottom-right causal alignment
-  }
-  if (r0 >= sq) return;  // row block past the end of its sequence (whole CTA)
-  const bool active1 = r1 < sq;
-  const int hk = h0 / p.group;
-  const uint32_t* kbits = p.key_bits ? p.key_bits + static_cast<size_t>(bz) * p.mask_words : nullptr;
-  int khi = kend;
-  if (p.causal) {
-    const int last_row = min((active1 ? r1 : r0) + kTileM - 1, sq - 1);
-    khi = min(khi, last_row + off + 1);
-  }
-  int j0 = 0, n_tiles = 0;
-  if (khi > klo) {
-    j0 = klo / kTileN;
-    n_tiles = (khi + kTileN - 1) / kTileN - j0;
-  }
+  const int n_units = p.n_rbu * p.units_per_rbu;
+  // The k-th unit of this CTA: units run heavy to light, so blocks of
+  // gridDim.x units are walked alternately forwards and backwards (the
+  // heaviest unit of one block pairs with the lightest of the next).
+  auto unit_index = [&](int k) {
+    const int G = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    return k * G + ((k & 1) ? (G - 1 - c) : c);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&s.bar_q, 1);
+    mbar_init(&s.q_free, 1);
     for (int i = 0; i < NS; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.v_full[i], 1);
@@ -217,8 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s.s_full[t], 1);
-      mbar_init(&s.p_full[t], 4);  // one arrival per softmax warp
+      mbar_init(&s.p_full[t], 4);   // one arrival per softmax warp
       mbar_init(&s.o_full[t], 1);
+      mbar_init(&s.o_empty[t], 4);  // the slot's softmax warps have read O
     }
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
@@ -235,41 +271,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &s.abort_flag;
   if (warp == 8) {
     // ------------------------------------------------------ TMA producer --
-    if (lane == 0 && n_tiles > 0) {
+    // K/V stages follow a tile counter g that runs across the CTA's units;
+    // the next unit's Q is loaded once the previous unit's last S product
+    // has read Q (q_free).
+    if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
       const uint64_t keep = policy_evict_last();
-      mbar_arrive_expect_tx(&s.bar_q, (active1 ? 2 : 1) * NB * kBoxBytes);
-      for (int cb = 0; cb < NB; ++cb) {
-        tma_load_3d(s.q[0][cb], &tq, &s.bar_q, cb * 64, qb + r0, bz * p.Hq + h0);
-        if (active1) tma_load_3d(s.q[1][cb], &tq, &s.bar_q, cb * 64, qb + r1, bz * p.Hq + h1);
-      }
-      const int zkv = bz * p.Hkv + hk;
-      int k_issued = 0, v_issued = 0;  // tiles whose loads were issued
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % NS;
-        const int use = j / NS;
-        const int c0 = (j0 + j) * kTileN;
-        // K tile j reuses the stage of K tile j - NS, read in round j - NS
-        if (use > 0 && !mbar_wait(&s.kv_free[st], (use - 1) & 1, abort_flag, kSiteKFree)) break;
-        mbar_arrive_expect_tx(&s.k_full[st], NB * kBoxBytes);
-        for (int cb = 0; cb < NB; ++cb)
-          tma_load_3d_hint(s.k[st][cb], &tk, &s.k_full[st], cb * 64, c0, zkv, keep);
-        k_issued = j + 1;
-        // V tile j reuses the stage of V tile j - NS, read in round j - NS + 1
-        if (use > 0) {
-          const int r = j - NS + 1;
-          if (!mbar_wait(&s.kv_free[r % NS], (r / NS) & 1, abort_flag, kSiteVFree)) break;
+      int g = 0, uq = 0;               // tiles and Q loads issued so far
+      int k_issued = 0, v_issued = 0;  // (global tile counts, for the abort drain)
+      bool ok = true;
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+        const int U = unit_index(k);
+        if (U >= n_units) continue;
+        const Unit un = unit_at(p, U);
+        if (un.n_tiles == 0) continue;
+        if (uq > 0 && !mbar_wait(&s.q_free, (uq - 1) & 1, abort_flag, kSiteQ)) break;
+        mbar_arrive_expect_tx(&s.bar_q, (un.active1 ? 2 : 1) * NB * kBoxBytes);
+        for (int cb = 0; cb < NB; ++cb) {
+          tma_load_3d(s.q[0][cb], &tq, &s.bar_q, cb * 64, un.qb + un.r0, un.bz * p.Hq + un.h0);
+          if (un.active1)
+            tma_load_3d(s.q[1][cb], &tq, &s.bar_q, cb * 64, un.qb + un.r1, un.bz * p.Hq + un.h1);
         }
-        mbar_arrive_expect_tx(&s.v_full[st], NB * kBoxBytes);
-        for (int cb = 0; cb < NB; ++cb)
-          tma_load_3d_hint(s.v[st][cb], &tv, &s.v_full[st], cb * 64, c0, zkv, keep);
-        v_issued = j + 1;
+        ++uq;
+        const int zkv = un.bz * p.Hkv + un.hk;
+        for (int j = 0; j < un.n_tiles; ++j, ++g) {
+          const int st = g % NS;
+          const int use = g / NS;
+          const int c0 = (un.j0 + j) * kTileN;
+          // stage st last held tile g - NS: its K was freed in round g - NS,
+          // its V in round g - NS + 1
+          if (use > 0 && !mbar_wait(&s.kv_free[st], (use - 1) & 1, abort_flag, kSiteKFree)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.k_full[st], NB * kBoxBytes);
+          for (int cb = 0; cb < NB; ++cb)
+            tma_load_3d_hint(s.k[st][cb], &tk, &s.k_full[st], cb * 64, c0, zkv, keep);
+          k_issued = g + 1;
+          if (use > 0) {
+            const int r = g - NS + 1;
+            if (!mbar_wait(&s.kv_free[r % NS], (r / NS) & 1, abort_flag, kSiteVFree)) {
+              ok = false;
+              break;
+            }
+          }
+          mbar_arrive_expect_tx(&s.v_full[st], NB * kBoxBytes);
+          for (int cb = 0; cb < NB; ++cb)
+            tma_load_3d_hint(s.v[st][cb], &tv, &s.v_full[st], cb * 64, c0, zkv, keep);
+          v_issued = g + 1;
+        }
       }
       if (*abort_flag) {
         // let every issued copy land before shared memory is released
-        mbar_drain(&s.bar_q, 0, kSiteDrain);
+        if (uq > 0) mbar_drain(&s.bar_q, (uq - 1) & 1, kSiteDrain);
         for (int j = max(0, k_issued - NS); j < k_issued; ++j)
           mbar_drain(&s.k_full[j % NS], (j / NS) & 1, kSiteDrain);
         for (int j = max(0, v_issued - NS); j < v_issued; ++j)
@@ -279,37 +335,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------- MMA issuer --
     // The whole warp runs this loop (warp-uniform control flow and operands);
-    // one elected lane issues each MMA and commit.
-    if (n_tiles > 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, false, true);
-      const int nslots = active1 ? 2 : 1;
-      // Descriptors are built once; each MMA only adds a compile-time offset.
-      constexpr uint32_t kStage = NB * kBoxBytes;  // bytes per K (or V) stage
-      const uint64_t qd0 = smem_desc_sw128(smem_u32(s.q[0][0]), 16, 1024);
-      const uint64_t qd1 = smem_desc_sw128(smem_u32(s.q[1][0]), 16, 1024);
-      const uint64_t kd0 = smem_desc_sw128(smem_u32(s.k[0][0]), 16, 1024);
-      const uint64_t vd0 = smem_desc_sw128(smem_u32(s.v[0][0]), NB > 1 ? kBoxBytes : 16u, 1024);
-      bool ok = mbar_wait_warp(&s.bar_q, 0, abort_flag, kSiteQ);
-      tc_fence_after();
-      for (int j = 0; ok && j <= n_tiles; ++j) {
+    // one elected lane issues each MMA and commit.  Per unit, round j issues
+    // PV_t(j-1) and S_t(j) for each active slot.  A unit's first S products
+    // run while the softmax warps still finish the previous unit's epilogue;
+    // its first PV into O_t waits until they have read O_t (o_empty).
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, false, true);
+    constexpr uint32_t kStage = NB * kBoxBytes;  // bytes per K (or V) stage
+    const uint64_t qd0 = smem_desc_sw128(smem_u32(s.q[0][0]), 16, 1024);
+    const uint64_t qd1 = smem_desc_sw128(smem_u32(s.q[1][0]), 16, 1024);
+    const uint64_t kd0 = smem_desc_sw128(smem_u32(s.k[0][0]), 16, 1024);
+    const uint64_t vd0 = smem_desc_sw128(smem_u32(s.v[0][0]), NB > 1 ? kBoxBytes : 16u, 1024);
+    int g = 0, uq = 0;
+    int ts[2] = {0, 0}, us[2] = {0, 0};  // per slot: tiles and units so far
+    bool ok = true;
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+      const int U = unit_index(k);
+      if (U >= n_units) continue;
+      const Unit un = unit_at(p, U);
+      if (un.n_tiles == 0) continue;
+      const int n = un.n_tiles;
+      const int nslots = un.active1 ? 2 : 1;
+      if (!mbar_wait_warp(&s.bar_q, uq & 1, abort_flag, kSiteQ)) break;
+      ++uq;
+      for (int j = 0; ok && j <= n; ++j) {
         // K and V arrive by TMA: the mbarrier wait alone orders those shared
         // memory writes before the MMAs (both sides are async-proxy accesses).
         // Only P, written by other threads' tcgen05.st, needs the tcgen05 fence.
-        if (j < n_tiles && !mbar_wait_warp(&s.k_full[j % NS], (j / NS) & 1, abort_flag, kSiteKFull))
+        const int gk = g + j, gv = g + j - 1;  // this round's K tile, V tile
+        if (j < n && !mbar_wait_warp(&s.k_full[gk % NS], (gk / NS) & 1, abort_flag, kSiteKFull)) {
+          ok = false;
           break;
-        const uint64_t kd = desc_add(kd0, static_cast<uint32_t>(j % NS) * kStage);
-        const uint64_t vd = desc_add(vd0, static_cast<uint32_t>((j + NS - 1) % NS) * kStage);
+        }
+        const uint64_t kd = desc_add(kd0, static_cast<uint32_t>(gk % NS) * kStage);
+        const uint64_t vd = desc_add(vd0, static_cast<uint32_t>(((gv % NS) + NS) % NS) * kStage);
         for (int t = 0; t < nslots; ++t) {
           const uint32_t t_s = tmem + t * kTileN;
           if (j > 0) {
             // O_t += P_t(j-1) V_{j-1}; P_t lives in the last 64 columns of S_t
-            if (!mbar_wait_warp(&s.p_full[t], (j - 1) & 1, abort_flag, kSitePFull)) {
-              ok = false;
-              break;
-            }
-            const int vs = (j - 1) % NS;
-            if (t == 0 && !mbar_wait_warp(&s.v_full[vs], ((j - 1) / NS) & 1, abort_flag, kSiteVFull)) {
+            if (!mbar_wait_warp(&s.p_full[t], (ts[t] + j - 1) & 1, abort_flag, kSitePFull) ||
+                (t == 0 &&
+                 !mbar_wait_warp(&s.v_full[gv % NS], (gv / NS) & 1, abort_flag, kSiteVFull)) ||
+                (j == 1 && us[t] > 0 &&
+                 !mbar_wait_warp(&s.o_empty[t], (us[t] - 1) & 1, abort_flag, kSiteOFull))) {
               ok = false;
               break;
             }
@@ -321,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 1; kk < kTileN / 16; ++kk)
               mma_ts_warp(t_o, t_p + kk * 8, desc_add(vd, kk * 16 * 128), idesc_pv, 1u);
           }
-          if (j < n_tiles) {
+          if (j < n) {
             // S_t = Q_t K_j^T
             const uint64_t qd = t ? qd1 : qd0;
 #pragma unroll
@@ -335,36 +403,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (j < n_tiles) mma_commit_warp(&s.kv_free[j % NS]);
+        if (j < n) mma_commit_warp(&s.kv_free[gk % NS]);
+        if (j == n - 1) mma_commit_warp(&s.q_free);  // the unit's last S has read Q
       }
-      if (warp_aborted(abort_flag)) {
-        // every MMA issued so far must finish before TMEM is released
-        mma_commit_warp(&s.drain);
-        mbar_drain(&s.drain, 0, kSiteDrain);
+      g += n;
+      for (int t = 0; t < nslots; ++t) {
+        ts[t] += n;
+        ++us[t];
       }
+    }
+    if (warp_aborted(abort_flag)) {
+      // every MMA issued so far must finish before TMEM is released
+      mma_commit_warp(&s.drain);
+      mbar_drain(&s.drain, 0, kSiteDrain);
     }
   } else {
     // ---------------------------------------------------- softmax warps --
     const int t = warp >> 2;
     const int row_in_tile = (warp & 3) * 32 + lane;
-    const int i = (t == 0 ? r0 : r1) + row_in_tile;
-    const int h = (t == 0) ? h0 : h1;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + t * kTileN + lane_off;
     const uint32_t t_o = tmem + 2 * kTileN + t * D + lane_off;
     const uint32_t t_p = t_s + kTileN / 2;  // P: bf16 pairs in S columns [64, 128)
-    const uint32_t bh = static_cast<uint32_t>(bz * p.Hq + h);  // dropout counter word 2
     const float c = p.scale_log2;
-    // keys visible to this row: [klo, khi_row)
-    int khi_row = kend;
-    if (p.causal) khi_row = min(khi_row, i + off + 1);
-    float m = neg_inf();  // running max of raw scores (unscaled)
-    float l = 0.f;        // running denominator, relative to 2^(m*c)
-    float lr = 0.f;       // same, over the bf16-rounded weights
-    bool ok = (t == 0) || active1;
-    if (ok && n_tiles > 0) {
+    int ts = 0, us = 0;  // this slot's tiles and units so far
+    bool ok = true;
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+      const int U = unit_index(k);
+      if (U >= n_units) continue;
+      const Unit un = unit_at(p, U);
+      if (!un.rows || (t == 1 && !un.active1)) continue;
+      const int n_tiles = un.n_tiles, j0 = un.j0, klo = un.klo, kend = un.kend;
+      const int sq = un.sq, qb = un.qb, bz = un.bz;
+      const int i = (t == 0 ? un.r0 : un.r1) + row_in_tile;
+      const int h = (t == 0) ? un.h0 : un.h1;
+      const uint32_t bh = static_cast<uint32_t>(bz * p.Hq + h);  // dropout counter word 2
+      const uint32_t* kbits =
+          p.key_bits ? p.key_bits + static_cast<size_t>(bz) * p.mask_words : nullptr;
+      // keys visible to this row: [klo, khi_row)
+      int khi_row = kend;
+      if (p.causal) khi_row = min(khi_row, i + un.off + 1);
+      float m = neg_inf();  // running max of raw scores (unscaled)
+      float l = 0.f;        // running denominator, relative to 2^(m*c)
+      float lr = 0.f;       // same, over the bf16-rounded weights
       for (int j = 0; j < n_tiles; ++j) {
-        if (!mbar_wait_warp(&s.s_full[t], j & 1, abort_flag, kSiteSFull)) { ok = false; break; }
+        if (!mbar_wait_warp(&s.s_full[t], (ts + j) & 1, abort_flag, kSiteSFull)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         uint32_t sr[kTileN];
 #pragma unroll
@@ -474,39 +560,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.p_full[t]);
       }
-      if (ok) ok = mbar_wait_warp(&s.o_full[t], 0, abort_flag, kSiteOFull);
-      tc_fence_after();
-    }
-    // ---- epilogue: O = u / l, LSE = m*scale + ln l ---------------------
-    if (((t == 0) || active1) && ok && !warp_aborted(abort_flag)) {
-      const bool live = l > 0.f;
-      const float inv = live ? (DROP ? p.drop.scale : 1.f) / lr : 0.f;
-      const bool in_range = i < sq;
-      const size_t row = (static_cast<size_t>(bz) * p.Hq + h) * p.Sq + qb + i;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t orr[32];
-        if (n_tiles > 0) {
-          tmem_ld32(t_o + cc * 32, orr);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int q2 = 0; q2 < 32; ++q2) orr[q2] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int q2 = 0; q2 < 16; ++q2)
-          pk[q2] = pack_bf16x2(__uint_as_float(orr[2 * q2]) * inv,
-                               __uint_as_float(orr[2 * q2 + 1]) * inv);
-        if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-          for (int q2 = 0; q2 < 4; ++q2)
-            dst[q2] = make_uint4(pk[4 * q2], pk[4 * q2 + 1], pk[4 * q2 + 2], pk[4 * q2 + 3]);
-        }
+      if (!ok) break;
+      if (n_tiles > 0) {
+        if (!mbar_wait_warp(&s.o_full[t], us & 1, abort_flag, kSiteOFull)) break;
+        tc_fence_after();
       }
-      if (in_range && p.lse) p.lse[row] = live ? fmaf(m, p.scale, logf(l)) : neg_inf();
+      if (warp_aborted(abort_flag)) break;
+      // ---- epilogue: O = u / lr, LSE = m*scale + ln l ----------------------
+      {
+        const bool live = l > 0.f;
+        const float inv = live ? (DROP ? p.drop.scale : 1.f) / lr : 0.f;
+        const bool in_range = i < sq;
+        const size_t row = (static_cast<size_t>(bz) * p.Hq + h) * p.Sq + qb + i;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t orr[32];
+          if (n_tiles > 0) {
+            tmem_ld32(t_o + cc * 32, orr);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int q2 = 0; q2 < 32; ++q2) orr[q2] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int q2 = 0; q2 < 16; ++q2)
+            pk[q2] = pack_bf16x2(__uint_as_float(orr[2 * q2]) * inv,
+                                 __uint_as_float(orr[2 * q2 + 1]) * inv);
+          if (in_range) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2)
+              dst[q2] = make_uint4(pk[4 * q2], pk[4 * q2 + 1], pk[4 * q2 + 2], pk[4 * q2 + 3]);
+          }
+        }
+        if (in_range && p.lse) p.lse[row] = live ? fmaf(m, p.scale, logf(l)) : neg_inf();
+      }
+      if (n_tiles > 0) {
+        // O_t has been read: the next unit's first PV may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.o_empty[t]);
+        ts += n_tiles;
+        ++us;
+      }
     }
   }
 
@@ -531,7 +629,14 @@ cudaError_t launch_fwd_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const unsigned int grid = static_cast<unsigned int>(p.n_rbu) * p.units_per_rbu;
+  // persistent: one CTA per SM (shared memory allows one), each walking the
+  // heavy-first unit list with stride gridDim.x
+  int dev = 0, n_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long units = static_cast<long long>(p.n_rbu) * p.units_per_rbu;
+  const unsigned int grid = static_cast<unsigned int>(std::min<long long>(units, n_sm));
   hook_before(stream);
   fa_fwd_kernel<D, MODE><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   hook_after(stream);
