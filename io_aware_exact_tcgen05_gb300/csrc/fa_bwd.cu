@@ -31,10 +31,19 @@
 // section (masked probabilities and their score gradients are 0); the same
 // mask, statistics and scale as the forward.
 //
+// The main kernel is persistent: one CTA per SM walks a fixed list of units
+// (key tile, KV head, batch row), heavy first and in alternating directions
+// block by block.  Per-tile barrier phases run on across units; the next
+// unit's K/V load waits for the current unit's last MMA (kv_empty) and its
+// first dV/dK products for the epilogue's TMEM reads (dkv_empty), so a unit's
+// drain and epilogue overlap the next unit's first tiles.
+//
 // Warp roles (448 threads): warps 0-7 compute (one key row = one TMEM lane per
 // thread; warps w and w+4 share the lanes of group w and split the 128 query
 // columns, so P and dS need no cross-warp exchange), warps 8-11 drain dQ (one
 // query row per thread), warp 12 TMA producer, warp 13 MMA issuer and TMEM owner.
+#include <algorithm>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -74,6 +83,7 @@ struct BwdSmem {
   uint64_t kv_full;
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_empty, dkv_full, drain;
+  uint64_t kv_empty, dkv_empty;  // hand-over between consecutive units
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -85,6 +95,56 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
+}
+
+// One work unit: a 128-key tile of one KV head of one batch row (or packed
+// sequence), walked against every query tile of the group's heads that sees
+// it.  Numbered key tile major, so under the causal rule the heaviest (tile
+// 0) come first.  Queries: logical rows [0, sq) from packed row qb of tensor
+// batch bz; keys [c0, c0 + 128) and the visible interval [klo, kend) are in
+// the K/V tensor's row coordinates, and keys at or past kseq belong to
+// another sequence (never stored).
+struct BwdUnit {
+  int b, hk, sq, qb, bz, klo, kend, kseq, off, c0, qt_lo, n_qt, n_it;
+  bool exists;  // the key tile lies inside its sequence
+};
+
+__device__ __forceinline__ BwdUnit bwd_unit_at(const BwdParams& p, int U) {
+  BwdUnit u;
+  const int bh = U % (p.grid_b * p.Hkv);
+  const int kt = U / (p.grid_b * p.Hkv);
+  u.b = bh / p.Hkv;
+  u.hk = bh % p.Hkv;
+  u.sq = p.Sq;
+  u.qb = 0;
+  u.bz = u.b;
+  if (p.cu_q) {  // packed ragged: b is the sequence
+    u.qb = max(0, min(p.cu_q[u.b], p.Sq));
+    u.sq = max(0, min(p.cu_q[u.b + 1], p.Sq) - u.qb);
+    u.klo = max(0, min(p.cu_k[u.b], p.Sk));
+    u.kend = max(u.klo, min(p.cu_k[u.b + 1], p.Sk));
+    u.kseq = u.kend;
+    u.off = u.kend - u.sq;
+    u.c0 = u.klo + kt * kTileN;
+    u.bz = 0;
+  } else {
+    u.klo = p.k_start ? p.k_start[u.b] : 0;
+    u.kend = p.k_end ? p.k_end[u.b] : p.Sk;
+    u.klo = max(0, min(u.klo, p.Sk));
+    u.kend = max(0, min(u.kend, p.Sk));
+    u.kseq = p.Sk;
+    u.off = p.Sk - p.Sq;
+    u.c0 = kt * kTileN;
+  }
+  u.exists = u.c0 < u.kseq;
+  const int n_qt_all = (u.sq + kTileM - 1) / kTileM;
+  u.qt_lo = 0;
+  if (p.causal) u.qt_lo = max(0, u.c0 - u.off) / kTileM;  // first query row that sees key c0
+  const bool keys_live = u.exists && (u.c0 < u.kend) && (u.c0 + kTileN > u.klo) &&
+                         (!p.causal || u.c0 - u.off < u.sq);
+  u.n_qt = keys_live ? max(0, n_qt_all - u.qt_lo) : 0;
+  u.n_it = u.n_qt * p.group;
+  return u;
 }
 
 // ------------------------------------------------------------ preprocess --
@@ -144,41 +204,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  // ---- work unit: key tile (heavy first under the causal rule), KV head, batch
-  const int bh = blockIdx.x % (p.grid_b * p.Hkv);
-  const int kt = blockIdx.x / (p.grid_b * p.Hkv);
-  const int b = bh / p.Hkv;
-  const int hk = bh % p.Hkv;
-  // This unit's queries: logical rows [0, sq) from packed row qb of tensor
-  // batch bz; its keys [c0, c0 + 128) and the visible interval [klo, kend)
-  // are in the K/V tensor's row coordinates, and keys at or past kseq belong
-  // to another sequence (never stored).
-  int sq = p.Sq, qb = 0, bz = b, klo, kend, kseq, off, c0;
-  if (p.cu_q) {  // packed ragged: b is the sequence
-    qb = max(0, min(p.cu_q[b], p.Sq));
-    sq = max(0, min(p.cu_q[b + 1], p.Sq) - qb);
-    klo = max(0, min(p.cu_k[b], p.Sk));
-    kend = max(klo, min(p.cu_k[b + 1], p.Sk));
-    kseq = kend;
-    off = kend - sq;
-    c0 = klo + kt * kTileN;
-    bz = 0;
-  } else {
-    klo = p.k_start ? p.k_start[b] : 0;
-    kend = p.k_end ? p.k_end[b] : p.Sk;
-    klo = max(0, min(klo, p.Sk));
-    kend = max(0, min(kend, p.Sk));
-    kseq = p.Sk;
-    off = p.Sk - p.Sq;
-    c0 = kt * kTileN;
-  }
-  if (c0 >= kseq) return;  // key tile past the end of its sequence (whole CTA)
-  const int n_qt_all = (sq + kTileM - 1) / kTileM;
-  int qt_lo = 0;
-  if (p.causal) qt_lo = max(0, c0 - off) / kTileM;  // first query row that sees key c0
-  const bool keys_live = (c0 < kend) && (c0 + kTileN > klo) && (!p.causal || c0 - off < sq);
-  const int n_qt = keys_live ? max(0, n_qt_all - qt_lo) : 0;
-  const int n_it = n_qt * p.group;
+  const int n_units = p.n_kt * p.grid_b * p.Hkv;
+  // The k-th unit of this CTA (units run heavy to light: key tile 0 first
+  // under the causal rule); blocks of gridDim.x units are walked alternately
+  // forwards and backwards so heavy and light units pair up.
+  auto unit_index = [&](int k) {
+    const int G = static_cast<int>(gridDim.x);
+    const int cb = static_cast<int>(blockIdx.x);
+    return k * G + ((k & 1) ? (G - 1 - cb) : cb);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&s.kv_full, 1);
@@ -193,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.dq_full, 1);
     mbar_init(&s.dq_empty, 4);  // one arrival per drain warp
     mbar_init(&s.dkv_full, 1);
+    mbar_init(&s.kv_empty, 1);   // the unit's last MMA has read K and V
+    mbar_init(&s.dkv_empty, 8);  // the compute warps have read dK and dV
     mbar_init(&s.drain, 1);
     mbar_init(&s.stat_ready[0], 4);
     mbar_init(&s.stat_ready[1], 4);
@@ -218,43 +254,62 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------ TMA producer --
-    if (lane == 0 && n_it > 0) {
+    // Q/dO stages follow an iteration counter that runs across the CTA's
+    // units; a unit's K/V load waits until the previous unit's last MMA has
+    // read K and V (kv_empty).
+    if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
       tma_prefetch_desc(&tdo);
-      const int zkv = bz * p.Hkv + hk;
-      mbar_arrive_expect_tx(&s.kv_full, 2 * NB * kBoxBytes);
-      for (int cb = 0; cb < NB; ++cb) {
-        tma_load_3d(s.k[cb], &tk, &s.kv_full, cb * 64, c0, zkv);
-        tma_load_3d(s.v[cb], &tv, &s.kv_full, cb * 64, c0, zkv);
-      }
+      int ig = 0, uk = 0;  // iterations and K/V loads issued so far
       int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int st = it % kQStages;
-        const int use = it / kQStages;
-        if (use > 0 && !mbar_wait(&s.q_empty[st], (use - 1) & 1, abort_flag, kSiteQEmpty)) break;
-        const int g = it / n_qt;
-        const int q0 = (qt_lo + it % n_qt) * kTileM;
-        const int zq = bz * p.Hq + hk * p.group + g;
-        mbar_arrive_expect_tx(&s.q_full[st], 2 * NB * kBoxBytes);
+      bool ok = true;
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+        const int U = unit_index(k);
+        if (U >= n_units) continue;
+        const BwdUnit un = bwd_unit_at(p, U);
+        if (!un.exists || un.n_it == 0) continue;
+        if (uk > 0 && !mbar_wait(&s.kv_empty, (uk - 1) & 1, abort_flag, kSiteKV)) break;
+        const int zkv = un.bz * p.Hkv + un.hk;
+        mbar_arrive_expect_tx(&s.kv_full, 2 * NB * kBoxBytes);
         for (int cb = 0; cb < NB; ++cb) {
-          tma_load_3d(s.q[st][cb], &tq, &s.q_full[st], cb * 64, qb + q0, zq);
-          tma_load_3d(s.dout[st][cb], &tdo, &s.q_full[st], cb * 64, qb + q0, zq);
+          tma_load_3d(s.k[cb], &tk, &s.kv_full, cb * 64, un.c0, zkv);
+          tma_load_3d(s.v[cb], &tv, &s.kv_full, cb * 64, un.c0, zkv);
         }
-        issued = it + 1;
+        ++uk;
+        for (int it = 0; it < un.n_it; ++it, ++ig) {
+          const int st = ig % kQStages;
+          const int use = ig / kQStages;
+          if (use > 0 && !mbar_wait(&s.q_empty[st], (use - 1) & 1, abort_flag, kSiteQEmpty)) {
+            ok = false;
+            break;
+          }
+          const int g = it / un.n_qt;
+          const int q0 = (un.qt_lo + it % un.n_qt) * kTileM;
+          const int zq = un.bz * p.Hq + un.hk * p.group + g;
+          mbar_arrive_expect_tx(&s.q_full[st], 2 * NB * kBoxBytes);
+          for (int cb = 0; cb < NB; ++cb) {
+            tma_load_3d(s.q[st][cb], &tq, &s.q_full[st], cb * 64, un.qb + q0, zq);
+            tma_load_3d(s.dout[st][cb], &tdo, &s.q_full[st], cb * 64, un.qb + q0, zq);
+          }
+          issued = ig + 1;
+        }
       }
       if (*abort_flag) {
-        mbar_drain(&s.kv_full, 0, kSiteDrain);
-        for (int it = max(0, issued - kQStages); it < issued; ++it)
-          mbar_drain(&s.q_full[it % kQStages], (it / kQStages) & 1, kSiteDrain);
+        if (uk > 0) mbar_drain(&s.kv_full, (uk - 1) & 1, kSiteDrain);
+        for (int i = max(0, issued - kQStages); i < issued; ++i)
+          mbar_drain(&s.q_full[i % kQStages], (i / kQStages) & 1, kSiteDrain);
       }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------- MMA issuer --
     // The whole warp runs this loop (warp-uniform control flow and operands);
-    // one elected lane issues each MMA and commit.
-    if (n_it > 0) {
+    // one elected lane issues each MMA and commit.  Per-tile barrier phases
+    // follow the iteration counter ig, which runs across the CTA's units; a
+    // unit's first dV/dK products (which overwrite the accumulators) wait
+    // until the previous unit's epilogue has read them (dkv_empty).
+    {
       constexpr uint32_t id_kq = idesc_bf16_f32(kTileN, kTileM, false, false);  // S^T, dP^T
       constexpr uint32_t id_acc = idesc_bf16_f32(kTileN, D, false, true);       // dV, dK
       constexpr uint32_t id_dq = idesc_bf16_f32(kTileM, D, true, true);         // dQ
@@ -269,56 +324,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_mn0 = smem_desc_sw128(smem_u32(s.q[0][0]), kLbo, 1024);
       const uint64_t o_mn0 = smem_desc_sw128(smem_u32(s.dout[0][0]), kLbo, 1024);
       const uint64_t ds_mn = smem_desc_sw128(smem_u32(s.ds[0]), kBoxBytes, 1024);
-      bool ok = mbar_wait_warp(&s.kv_full, 0, abort_flag, kSiteKV);
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int st = it % kQStages;
-        const uint32_t so = static_cast<uint32_t>(st) * kStage;
-        // Q and dO arrive by TMA (the mbarrier wait orders them before the
-        // MMAs); the S^T columns this overwrites were last touched by other
-        // threads before p_full of the previous tile, whose fence covers them.
-        if (!mbar_wait_warp(&s.q_full[st], (it / kQStages) & 1, abort_flag, kSiteQFull)) break;
-        // S^T = K Q^T  (A = K rows, B = Q rows, both K-major over d)
+      int ig = 0, uk = 0;
+      bool ok = true;
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+        const int U = unit_index(k);
+        if (U >= n_units) continue;
+        const BwdUnit un = bwd_unit_at(p, U);
+        if (!un.exists || un.n_it == 0) continue;
+        if (!mbar_wait_warp(&s.kv_full, uk & 1, abort_flag, kSiteKV)) break;
+        for (int it = 0; ok && it < un.n_it; ++it, ++ig) {
+          const int st = ig % kQStages;
+          const uint32_t so = static_cast<uint32_t>(st) * kStage;
+          // Q and dO arrive by TMA (the mbarrier wait orders them before the
+          // MMAs); the S^T columns this overwrites were last touched by other
+          // threads before p_full of the previous tile, whose fence covers them.
+          if (!mbar_wait_warp(&s.q_full[st], (ig / kQStages) & 1, abort_flag, kSiteQFull)) {
+            ok = false;
+            break;
+          }
+          // S^T = K Q^T  (A = K rows, B = Q rows, both K-major over d)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss_warp(t_S, desc_add(k_kmaj, off), desc_add(q_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_ss_warp(t_S, desc_add(k_kmaj, off), desc_add(q_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_warp(&s.s_full);
+          // dP^T = V dO^T; its columns held dQ of the previous tile
+          if (ig > 0 && !mbar_wait_warp(&s.dq_empty, (ig - 1) & 1, abort_flag, kSiteDQEmpty)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_ss_warp(t_dP, desc_add(v_kmaj, off), desc_add(o_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_warp(&s.dp_full);
+          // dV += P^T dO  (A = P^T in TMEM; B = dO rows, MN-major over d)
+          if (!mbar_wait_warp(&s.p_full, ig & 1, abort_flag, kSiteP) ||
+              (it == 0 && uk > 0 &&
+               !mbar_wait_warp(&s.dkv_empty, (uk - 1) & 1, abort_flag, kSiteDKV))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_ts_warp(t_dV, t_S, desc_add(o_mn0, so), id_acc, it > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 1; kk < kTileM / 16; ++kk)
+            mma_ts_warp(t_dV, t_S + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(o_mn0, so + kk * 2048),
+                   id_acc, 1u);
+          // dK += dS^T Q  (A = dS^T in TMEM; B = Q rows, MN-major over d)
+          if (!mbar_wait_warp(&s.ds_full, ig & 1, abort_flag, kSiteDS)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_ts_warp(t_dK, t_dP, desc_add(q_mn0, so), id_acc, it > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 1; kk < kTileM / 16; ++kk)
+            mma_ts_warp(t_dK, t_dP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(q_mn0, so + kk * 2048),
+                   id_acc, 1u);
+          // dQ = dS K  (A = dS: shared rows = keys, queries contiguous -> MN-major;
+          //             B = K rows, d contiguous -> MN-major), into the dP^T columns
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ss_warp(t_dP, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), id_dq,
+                   kk > 0 ? 1u : 0u);
+          mma_commit_warp(&s.dq_full);
+          mma_commit_warp(&s.q_empty[st]);
         }
-        mma_commit_warp(&s.s_full);
-        // dP^T = V dO^T; its columns held dQ of the previous tile
-        if (it > 0 && !mbar_wait_warp(&s.dq_empty, (it - 1) & 1, abort_flag, kSiteDQEmpty)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss_warp(t_dP, desc_add(v_kmaj, off), desc_add(o_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_warp(&s.dp_full);
-        // dV += P^T dO  (A = P^T in TMEM; B = dO rows, MN-major over d)
-        if (!mbar_wait_warp(&s.p_full, it & 1, abort_flag, kSiteP)) break;
-        tc_fence_after();
-        mma_ts_warp(t_dV, t_S, desc_add(o_mn0, so), id_acc, it > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 1; kk < kTileM / 16; ++kk)
-          mma_ts_warp(t_dV, t_S + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(o_mn0, so + kk * 2048),
-                 id_acc, 1u);
-        // dK += dS^T Q  (A = dS^T in TMEM; B = Q rows, MN-major over d)
-        if (!mbar_wait_warp(&s.ds_full, it & 1, abort_flag, kSiteDS)) break;
-        tc_fence_after();
-        mma_ts_warp(t_dK, t_dP, desc_add(q_mn0, so), id_acc, it > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 1; kk < kTileM / 16; ++kk)
-          mma_ts_warp(t_dK, t_dP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(q_mn0, so + kk * 2048),
-                 id_acc, 1u);
-        // dQ = dS K  (A = dS: shared rows = keys, queries contiguous -> MN-major;
-        //             B = K rows, d contiguous -> MN-major), into the dP^T columns
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ss_warp(t_dP, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), id_dq,
-                 kk > 0 ? 1u : 0u);
-        mma_commit_warp(&s.dq_full);
-        mma_commit_warp(&s.q_empty[st]);
+        if (!ok) break;
+        mma_commit_warp(&s.dkv_full);
+        mma_commit_warp(&s.kv_empty);  // the unit's last MMA has read K and V
+        ++uk;
       }
-      mma_commit_warp(&s.dkv_full);
       if (warp_aborted(abort_flag)) {
         mma_commit_warp(&s.drain);
         mbar_drain(&s.drain, 0, kSiteDrain);
@@ -329,13 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = warp & 3;           // TMEM lane group
     const int hf = warp >> 2;           // query columns [64 hf, 64 hf + 64)
     const int row = grp * 32 + lane;    // key row in the tile = TMEM lane
-    const int key = c0 + row;
     const uint32_t lane_off = static_cast<uint32_t>(grp * 32) << 16;
-    bool key_in = key >= klo && key < kend;
-    if (p.key_bits && key_in) {
-      const uint32_t w = __ldg(p.key_bits + static_cast<size_t>(bz) * p.mask_words + key / 32);
-      key_in = (w >> (key & 31)) & 1u;
-    }
     const float c = p.scale_log2;
     const uint32_t ds_base = smem_u32(s.ds[0]);
     // dropout: the four lanes of keys 4a..4a+3 share a Philox counter per
@@ -343,173 +417,200 @@ __global__ void __launch_bounds__(kThreads, 1)
     // group draws query t = l & 3 of each block of 4 and ballots hand every
     // lane its own key's bits
     const uint32_t grp4 = static_cast<uint32_t>(lane & ~3);
-    const uint32_t key4 = static_cast<uint32_t>(key) >> 2;
+    int ig = 0, uk = 0;  // iterations and units with work, across the CTA's units
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int g = it / n_qt;
-      const int q0 = (qt_lo + it % n_qt) * kTileM;
-      const int h = hk * p.group + g;
-      // Row statistics of this query tile, staged by the hf = 0 warps in the
-      // buffer of this tile's parity.  A buffer is rewritten two tiles later,
-      // after every compute warp has signalled dS of the tile that read it
-      // (S^T of the next tile is issued only after that).
-      const int sb = it & 1;
-      if (hf == 0) {
-        // stored negated so that p = 2^(s*c + nl) and dP - D = dP + nd are one
-        // packed FMA / add per pair; rows without keys get nl = -inf (p = 0)
-        const int qi = q0 + row;
-        float nl = neg_inf(), nd = 0.f;
-        if (qi < sq) {
-          const size_t ri = (static_cast<size_t>(bz) * p.Hq + h) * p.Sq + qb + qi;
-          const float lse = p.lse[ri];
-          nl = (lse == neg_inf()) ? neg_inf() : -lse * 1.4426950408889634f;
-          nd = -p.delta[ri];
-        }
-        s.nlse2[sb][row] = nl;
-        s.ndelta[sb][row] = nd;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.stat_ready[sb]);
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+      const int U = unit_index(k);
+      if (U >= n_units) continue;
+      const BwdUnit un = bwd_unit_at(p, U);
+      if (!un.exists) continue;
+      const int c0 = un.c0, klo = un.klo, kend = un.kend, kseq = un.kseq, sq = un.sq;
+      const int qb = un.qb, bz = un.bz, off = un.off, qt_lo = un.qt_lo, n_qt = un.n_qt;
+      const int n_it = un.n_it, hk = un.hk;
+      const int key = c0 + row;
+      bool key_in = key >= klo && key < kend;
+      if (p.key_bits && key_in) {
+        const uint32_t w = __ldg(p.key_bits + static_cast<size_t>(bz) * p.mask_words + key / 32);
+        key_in = (w >> (key & 31)) & 1u;
       }
-      if (!mbar_wait_warp(&s.stat_ready[sb], (it >> 1) & 1, abort_flag, kSiteStat)) { ok = false; break; }
-      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(s.nlse2[sb]);
-      const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(s.ndelta[sb]);
-      const uint64_t c2 = f2_pack(c, c);
-      // visible queries of this key row: q >= key - off (causal), key in [klo, kend)
-      const int qmin = p.causal ? key - off : -0x7fffffff;
-      const bool need_mask = !key_in || (p.causal && q0 + hf * 64 < qmin);
-      if (!mbar_wait_warp(&s.s_full, it & 1, abort_flag, kSiteS)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t pk[32];  // this half's P^T, bf16 pairs
-      uint32_t keepw[2] = {~0u, ~0u};  // dropout: bit q = query hf*64 + 32 cc + q kept
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t sr[32];
-        tmem_ld32(t_S + lane_off + hf * 64 + cc * 32, sr);
-        if (DROP) {
-          const uint32_t bh = static_cast<uint32_t>(bz * p.Hq + h);
-          uint32_t kw = 0;
-#pragma unroll
-          for (int g4 = 0; g4 < 8; ++g4) {
-            const uint32_t qi = static_cast<uint32_t>(q0 + hf * 64 + cc * 32 + g4 * 4) +
-                                static_cast<uint32_t>(lane & 3);
-            const uint32_t k4 = dropout_keep4(p.drop, key4, qi, bh);
-            const uint32_t b0 = __ballot_sync(0xffffffffu, k4 & 1u);
-            const uint32_t b1 = __ballot_sync(0xffffffffu, k4 & 2u);
-            const uint32_t b2 = __ballot_sync(0xffffffffu, k4 & 4u);
-            const uint32_t b3 = __ballot_sync(0xffffffffu, k4 & 8u);
-            const uint32_t sel = (lane & 2) ? ((lane & 1) ? b3 : b2) : ((lane & 1) ? b1 : b0);
-            kw |= ((sel >> grp4) & 0xFu) << (4 * g4);
+      const uint32_t key4 = static_cast<uint32_t>(key) >> 2;
+      for (int it = 0; it < n_it; ++it) {
+        const int gi = ig + it;  // this iteration's index across units (barrier phases)
+        const int g = it / n_qt;
+        const int q0 = (qt_lo + it % n_qt) * kTileM;
+        const int h = hk * p.group + g;
+        // Row statistics of this query tile, staged by the hf = 0 warps in the
+        // buffer of this tile's parity.  A buffer is rewritten two tiles later,
+        // after every compute warp has signalled dS of the tile that read it
+        // (S^T of the next tile is issued only after that).
+        const int sb = gi & 1;
+        if (hf == 0) {
+          // stored negated so that p = 2^(s*c + nl) and dP - D = dP + nd are one
+          // packed FMA / add per pair; rows without keys get nl = -inf (p = 0)
+          const int qi = q0 + row;
+          float nl = neg_inf(), nd = 0.f;
+          if (qi < sq) {
+            const size_t ri = (static_cast<size_t>(bz) * p.Hq + h) * p.Sq + qb + qi;
+            const float lse = p.lse[ri];
+            nl = (lse == neg_inf()) ? neg_inf() : -lse * 1.4426950408889634f;
+            nd = -p.delta[ri];
           }
-          keepw[cc] = kw;
+          s.nlse2[sb][row] = nl;
+          s.ndelta[sb][row] = nd;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.stat_ready[sb]);
         }
-        tmem_wait_ld();
-        uint32_t pw[16];
+        if (!mbar_wait_warp(&s.stat_ready[sb], (gi >> 1) & 1, abort_flag, kSiteStat)) { ok = false; break; }
+        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(s.nlse2[sb]);
+        const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(s.ndelta[sb]);
+        const uint64_t c2 = f2_pack(c, c);
+        // visible queries of this key row: q >= key - off (causal), key in [klo, kend)
+        const int qmin = p.causal ? key - off : -0x7fffffff;
+        const bool need_mask = !key_in || (p.causal && q0 + hf * 64 < qmin);
+        if (!mbar_wait_warp(&s.s_full, gi & 1, abort_flag, kSiteS)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t pk[32];  // this half's P^T, bf16 pairs
+        uint32_t keepw[2] = {~0u, ~0u};  // dropout: bit q = query hf*64 + 32 cc + q kept
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int qa = hf * 64 + cc * 32 + 2 * e;
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), c2,
-                           nl2[qa >> 1]),
-                    x0, x1);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
-          if (need_mask) {
-            if (!key_in || q0 + qa < qmin) p0 = 0.f;
-            if (!key_in || q0 + qa + 1 < qmin) p1 = 0.f;
-          }
-          pk[cc * 16 + e] = pack_bf16x2(p0, p1);
-          pw[e] = pk[cc * 16 + e];
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t sr[32];
+          tmem_ld32(t_S + lane_off + hf * 64 + cc * 32, sr);
           if (DROP) {
-            const uint32_t kb = keepw[cc] >> (2 * e);
-            pw[e] &= ((kb & 1u) ? 0x0000ffffu : 0u) | ((kb & 2u) ? 0xffff0000u : 0u);
+            const uint32_t bh = static_cast<uint32_t>(bz * p.Hq + h);
+            uint32_t kw = 0;
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4) {
+              const uint32_t qi = static_cast<uint32_t>(q0 + hf * 64 + cc * 32 + g4 * 4) +
+                                  static_cast<uint32_t>(lane & 3);
+              const uint32_t k4 = dropout_keep4(p.drop, key4, qi, bh);
+              const uint32_t b0 = __ballot_sync(0xffffffffu, k4 & 1u);
+              const uint32_t b1 = __ballot_sync(0xffffffffu, k4 & 2u);
+              const uint32_t b2 = __ballot_sync(0xffffffffu, k4 & 4u);
+              const uint32_t b3 = __ballot_sync(0xffffffffu, k4 & 8u);
+              const uint32_t sel = (lane & 2) ? ((lane & 1) ? b3 : b2) : ((lane & 1) ? b1 : b0);
+              kw |= ((sel >> grp4) & 0xFu) << (4 * g4);
+            }
+            keepw[cc] = kw;
           }
-        }
-        // P columns [64 hf + 16 cc, +16) hold scores this warp already loaded
-        tmem_st16(t_S + lane_off + hf * 64 + cc * 16, pw);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.p_full);
-      // dS^T = P^T * (dP^T - D)
-      if (!mbar_wait_warp(&s.dp_full, it & 1, abort_flag, kSiteDP)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t blk = ds_base + hf * (kTileN * 128) + row * 128;  // query block hf
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t dr[32];
-        tmem_ld32(t_dP + lane_off + hf * 64 + cc * 32, dr);
-        tmem_wait_ld();
-        uint32_t dw[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int qa = hf * 64 + cc * 32 + 2 * e;
-          uint64_t dp2;
-          if (DROP) {  // dP of the dropped weights: keep / (1 - p) * <dO, v>
-            const uint32_t kb = keepw[cc] >> (2 * e);
-            dp2 = f2_fma(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
-                         f2_pack((kb & 1u) ? p.drop.scale : 0.f, (kb & 2u) ? p.drop.scale : 0.f),
-                         nd2[qa >> 1]);
-          } else {
-            dp2 = f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
-                         nd2[qa >> 1]);
-          }
-          float d0, d1;
-          f2_unpack(f2_mul(bf16x2_to_f2(pk[cc * 16 + e]), dp2), d0, d1);
-          dw[e] = pack_bf16x2(d0, d1);
-        }
-        tmem_st16(t_dP + lane_off + hf * 64 + cc * 16, dw);
-        // shared copy: 32 queries = four 16-byte chunks of query block hf
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const uint32_t chunk = static_cast<uint32_t>((cc * 4 + ch) ^ (row & 7));
-          st_shared_v4(blk + chunk * 16, dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
-        }
-      }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.ds_full);
-    }
-    // ---- epilogue: dK = scale * acc, dV = acc for head-dim columns
-    //      [D/2 hf, D/2 hf + D/2)  (zeros when no query sees the keys)
-    if (ok && n_it > 0) ok = mbar_wait_warp(&s.dkv_full, 0, abort_flag, kSiteDKV);
-    tc_fence_after();
-    // warp-uniform: the TMEM loads below are warp-collective, only the stores
-    // depend on the lane's key
-    if (ok && !warp_aborted(abort_flag)) {
-      const bool store = key < kseq;
-      const size_t kr = (static_cast<size_t>(bz) * p.Hkv + hk) * p.Sk + key;
-      __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
-      __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
-#pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {
-        const uint32_t src = (pass == 0) ? t_dK : t_dV;
-        const float mul = (pass == 0) ? p.scale : (DROP ? p.drop.scale : 1.f);
-        __nv_bfloat16* dst = (pass == 0) ? dkrow : dvrow;
-#pragma unroll
-        for (int c2i = 0; c2i < D / 64; ++c2i) {
-          const int cc = hf * (D / 64) + c2i;  // 32-column chunk of the head dimension
-          uint32_t r[32];
-          if (n_it > 0) {
-            tmem_ld32(src + lane_off + cc * 32, r);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = 0u;
-          }
+          tmem_wait_ld();
           uint32_t pw[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pw[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-          if (store) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+          for (int e = 0; e < 16; ++e) {
+            const int qa = hf * 64 + cc * 32 + 2 * e;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), c2,
+                             nl2[qa >> 1]),
+                      x0, x1);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
+            if (need_mask) {
+              if (!key_in || q0 + qa < qmin) p0 = 0.f;
+              if (!key_in || q0 + qa + 1 < qmin) p1 = 0.f;
+            }
+            pk[cc * 16 + e] = pack_bf16x2(p0, p1);
+            pw[e] = pk[cc * 16 + e];
+            if (DROP) {
+              const uint32_t kb = keepw[cc] >> (2 * e);
+              pw[e] &= ((kb & 1u) ? 0x0000ffffu : 0u) | ((kb & 2u) ? 0xffff0000u : 0u);
+            }
+          }
+          // P columns [64 hf + 16 cc, +16) hold scores this warp already loaded
+          tmem_st16(t_S + lane_off + hf * 64 + cc * 16, pw);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.p_full);
+        // dS^T = P^T * (dP^T - D)
+        if (!mbar_wait_warp(&s.dp_full, gi & 1, abort_flag, kSiteDP)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t blk = ds_base + hf * (kTileN * 128) + row * 128;  // query block hf
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              d4[e] = make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t dr[32];
+          tmem_ld32(t_dP + lane_off + hf * 64 + cc * 32, dr);
+          tmem_wait_ld();
+          uint32_t dw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int qa = hf * 64 + cc * 32 + 2 * e;
+            uint64_t dp2;
+            if (DROP) {  // dP of the dropped weights: keep / (1 - p) * <dO, v>
+              const uint32_t kb = keepw[cc] >> (2 * e);
+              dp2 = f2_fma(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
+                           f2_pack((kb & 1u) ? p.drop.scale : 0.f, (kb & 2u) ? p.drop.scale : 0.f),
+                           nd2[qa >> 1]);
+            } else {
+              dp2 = f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
+                           nd2[qa >> 1]);
+            }
+            float d0, d1;
+            f2_unpack(f2_mul(bf16x2_to_f2(pk[cc * 16 + e]), dp2), d0, d1);
+            dw[e] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(t_dP + lane_off + hf * 64 + cc * 16, dw);
+          // shared copy: 32 queries = four 16-byte chunks of query block hf
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint32_t chunk = static_cast<uint32_t>((cc * 4 + ch) ^ (row & 7));
+            st_shared_v4(blk + chunk * 16, dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
           }
         }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.ds_full);
+      }
+      // ---- epilogue: dK = scale * acc, dV = acc for head-dim columns
+      //      [D/2 hf, D/2 hf + D/2)  (zeros when no query sees the keys)
+      if (!ok) break;
+      if (n_it > 0 && !mbar_wait_warp(&s.dkv_full, uk & 1, abort_flag, kSiteDKV)) break;
+      tc_fence_after();
+      if (warp_aborted(abort_flag)) break;
+      // warp-uniform: the TMEM loads below are warp-collective, only the stores
+      // depend on the lane's key
+      {
+        const bool store = key < kseq;
+        const size_t kr = (static_cast<size_t>(bz) * p.Hkv + hk) * p.Sk + key;
+        __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
+        __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          const uint32_t src = (pass == 0) ? t_dK : t_dV;
+          const float mul = (pass == 0) ? p.scale : (DROP ? p.drop.scale : 1.f);
+          __nv_bfloat16* dst = (pass == 0) ? dkrow : dvrow;
+#pragma unroll
+          for (int c2i = 0; c2i < D / 64; ++c2i) {
+            const int cc = hf * (D / 64) + c2i;  // 32-column chunk of the head dimension
+            uint32_t r[32];
+            if (n_it > 0) {
+              tmem_ld32(src + lane_off + cc * 32, r);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = 0u;
+            }
+            uint32_t pw[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pw[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+            if (store) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                d4[e] = make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
+            }
+          }
+        }
+      }
+      if (n_it > 0) {
+        // dK and dV have been read: the next unit's first products may overwrite them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.dkv_empty);
+        ig += n_it;
+        ++uk;
       }
     }
   } else if (warp < 12) {
@@ -521,43 +622,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     constexpr int kSlice = 32 * D * 4;  // bytes of one warp's rows
-    for (int it = 0; it < n_it; ++it) {
-      const int g = it / n_qt;
-      const int q0 = (qt_lo + it % n_qt) * kTileM;
-      const int h = hk * p.group + g;
-      const int st = it % kQStages;
-      unsigned char* region = reinterpret_cast<unsigned char*>(
-                                  wq < 2 ? &s.q[st][0][0] : &s.dout[st][0][0]) +
-                              (wq & 1) * kSlice;
-      const uint32_t region_u32 = smem_u32(region);
-      if (!mbar_wait_warp(&s.dq_full, it & 1, abort_flag, kSiteDQFull)) break;
-      tc_fence_after();
+    int ig = 0;  // iterations across the CTA's units (barrier phases, stages)
+    bool ok = true;
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+      const int U = unit_index(k);
+      if (U >= n_units) continue;
+      const BwdUnit un = bwd_unit_at(p, U);
+      if (!un.exists || un.n_it == 0) continue;
+      for (int it = 0; it < un.n_it; ++it, ++ig) {
+        const int g = it / un.n_qt;
+        const int q0 = (un.qt_lo + it % un.n_qt) * kTileM;
+        const int h = un.hk * p.group + g;
+        const int st = ig % kQStages;
+        unsigned char* region = reinterpret_cast<unsigned char*>(
+                                    wq < 2 ? &s.q[st][0][0] : &s.dout[st][0][0]) +
+                                (wq & 1) * kSlice;
+        const uint32_t region_u32 = smem_u32(region);
+        if (!mbar_wait_warp(&s.dq_full, ig & 1, abort_flag, kSiteDQFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
-      for (int bx = 0; bx < D / 32; ++bx) {
-        uint32_t r[32];
-        tmem_ld32(t_dP + lane_off + bx * 32, r);
-        tmem_wait_ld();
-        const uint32_t base = region_u32 + bx * 4096 + lane * 128;
+        for (int bx = 0; bx < D / 32; ++bx) {
+          uint32_t r[32];
+          tmem_ld32(t_dP + lane_off + bx * 32, r);
+          tmem_wait_ld();
+          const uint32_t base = region_u32 + bx * 4096 + lane * 128;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(base + ((ch ^ (lane & 7)) * 16), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2],
-                       r[4 * ch + 3]);
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(base + ((ch ^ (lane & 7)) * 16), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2],
+                         r[4 * ch + 3]);
+        }
+        // dQ is out of TMEM: dP^T of the next tile may reuse the columns
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.dq_empty);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int bx = 0; bx < D / 32; ++bx)
+            tma_reduce_add_3d(&tdq, region + bx * 4096, bx * 32, un.qb + q0 + wq * 32,
+                              un.bz * p.Hq + h);
+          bulk_commit_group();
+          bulk_wait_read0();
+          mbar_arrive(&s.q_empty[st]);
+        }
+        __syncwarp();
       }
-      // dQ is out of TMEM: dP^T of the next tile may reuse the columns
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.dq_empty);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-#pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx)
-          tma_reduce_add_3d(&tdq, region + bx * 4096, bx * 32, qb + q0 + wq * 32, bz * p.Hq + h);
-        bulk_commit_group();
-        bulk_wait_read0();
-        mbar_arrive(&s.q_empty[st]);
-      }
-      __syncwarp();
     }
     if (lane == 0) bulk_wait0();  // reduces complete before the CTA leaves
   }
@@ -590,7 +703,13 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   fa_bwd_pre<D><<<static_cast<unsigned int>((pre_threads + 255) / 256), 256, 0, stream>>>(p, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned int grid = static_cast<unsigned int>(p.n_kt) * p.grid_b * p.Hkv;
+  // persistent: one CTA per SM (shared memory allows one) over the unit list
+  int dev = 0, n_sm = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long units = static_cast<long long>(p.n_kt) * p.grid_b * p.Hkv;
+  const unsigned int grid = static_cast<unsigned int>(std::min<long long>(units, n_sm));
   if (grid > 0) {  // packed sequences that all lack keys: dQ stays zero
     hook_before(stream);
     if (drop)
