@@ -30,8 +30,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
       k0 += kWeyl0;
       k1 += kWeyl1;
     }
-    const uint32_t hi_a = __umulhi(kMulA, c.x), lo_a = kMulA * c.x;
-    const uint32_t hi_b = __umulhi(kMulB, c.z), lo_b = kMulB * c.z;
+    // one 32 x 32 -> 64-bit product gives both halves
+    const uint64_t pa = static_cast<uint64_t>(kMulA) * c.x;
+    const uint64_t pb = static_cast<uint64_t>(kMulB) * c.z;
+    const uint32_t hi_a = static_cast<uint32_t>(pa >> 32), lo_a = static_cast<uint32_t>(pa);
+    const uint32_t hi_b = static_cast<uint32_t>(pb >> 32), lo_b = static_cast<uint32_t>(pb);
     c = make_uint4(hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a);
   }
   return c;
