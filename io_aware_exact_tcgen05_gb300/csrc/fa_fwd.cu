@@ -635,8 +635,12 @@ cudaError_t launch_fwd_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  // Packed ragged batches keep one unit per CTA: their unit costs vary with
+  // the sequence lengths, which only the hardware's dynamic CTA scheduling
+  // balances (with gridDim.x = units every CTA's sequence is just its own unit).
   const long long units = static_cast<long long>(p.n_rbu) * p.units_per_rbu;
-  const unsigned int grid = static_cast<unsigned int>(std::min<long long>(units, n_sm));
+  const unsigned int grid =
+      static_cast<unsigned int>(p.cu_q ? units : std::min<long long>(units, n_sm));
   hook_before(stream);
   fa_fwd_kernel<D, MODE><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   hook_after(stream);
