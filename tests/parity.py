@@ -1,6 +1,6 @@
 """Shared helpers for the GPU-vs-oracle parity tests (test infrastructure).
 
-Tolerances (stated in the spec acceptance rule and applied per tensor):
+Tolerances (the stated acceptance rule, applied per tensor):
   O:           max |gpu - oracle| <= 2e-2
   LSE:         max |gpu - oracle| <= 1e-3 on finite entries; -inf must match exactly
   dQ, dK, dV:  max |gpu - oracle| <= 5e-2 * max |oracle|   (per tensor)
