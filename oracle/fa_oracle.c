@@ -335,6 +335,48 @@ int oracle_probs(const void* q, const void* k, const void* v, const void* dout, 
 }
 
 /*
+ * dQ_i of one query row (flat row id), from its own statistics: m_i, l_i and
+ * O_i from the definition, D_i = <dO_i, O_i>, then dQ_i = scale sum over
+ * visible j of p_ij (dP_ij - D_i) k_j.  Writes dqr[d]; returns m_i, l_i, D_i.
+ * s, qrow, dorow, u, orow are caller scratch.
+ */
+static void dq_row(src_t qs, src_t kk, src_t vv, src_t dos, long flat, long B, long Hq,
+                   long Hkv, long Sq, long Sk, long d, int causal, double scale,
+                   const int* k_start, const int* k_end, const unsigned char* key_mask,
+                   const drop_t* dr, double* s, double* qrow, double* dorow, double* u,
+                   double* orow, double* dqr, double* m_out, double* l_out, double* D_out) {
+  const long group = Hq / Hkv;
+  const long i = flat % Sq;
+  const long h = (flat / Sq) % Hq;
+  const long b = flat / (Sq * Hq);
+  (void)B;
+  const long kvbase = (b * Hkv + h / group) * Sk * d;
+  long ks, ke;
+  key_range(k_start, k_end, b, Sk, &ks, &ke);
+  load_row(qs, flat * d, d, qrow);
+  load_row(dos, flat * d, d, dorow);
+  double lse, m, l;
+  const unsigned char* km = mask_row(key_mask, b, Sk);
+  row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, km, dr,
+                b * Hq + h, s, &m, &l, u, orow, &lse);
+  double D = 0.0;
+  for (long c = 0; c < d; ++c) D += dorow[c] * orow[c];
+  for (long c = 0; c < d; ++c) dqr[c] = 0.0;
+  *m_out = m;
+  *l_out = l;
+  *D_out = D;
+  if (l <= 0.0) return;
+  for (long j = 0; j < Sk; ++j) {
+    if (!is_visible(i, j, Sq, Sk, causal, ks, ke, km)) continue;
+    const double pij = exp(s[j] - m) / l;
+    double dp = 0.0;
+    for (long c = 0; c < d; ++c) dp += dorow[c] * ld(vv, kvbase + j * d + c);
+    const double dsij = pij * (dp * drop_factor(dr, b * Hq + h, i, j) - D);
+    for (long c = 0; c < d; ++c) dqr[c] += scale * dsij * ld(kk, kvbase + j * d + c);
+  }
+}
+
+/*
  * Full backward: dq[B,Hq,Sq,d], dk/dv[B,Hkv,Sk,d], all fp64.
  * Per-row statistics m_i, l_i and D_i are formed first from the definition;
  * every p_ij and dS_ij is then evaluated from them where it is needed.
@@ -368,34 +410,10 @@ int oracle_bwd(const void* q, const void* k, const void* v, const void* dout, in
       err = 1;
     } else {
 #pragma omp for schedule(dynamic, 16)
-      for (long flat = 0; flat < nrow; ++flat) {
-        const long i = flat % Sq;
-        const long h = (flat / Sq) % Hq;
-        const long b = flat / (Sq * Hq);
-        const long kvbase = (b * Hkv + h / group) * Sk * d;
-        long ks, ke;
-        key_range(k_start, k_end, b, Sk, &ks, &ke);
-        load_row(qs, flat * d, d, qrow);
-        load_row(dos, flat * d, d, dorow);
-        double lse;
-        const unsigned char* km = mask_row(key_mask, b, Sk);
-        row_attention(qrow, kk, kvbase, vv, kvbase, Sk, d, scale, i, Sq, causal, ks, ke, km, &dr,
-                      b * Hq + h, s, &M[flat], &L[flat], u, orow, &lse);
-        double D = 0.0;
-        for (long c = 0; c < d; ++c) D += dorow[c] * orow[c];
-        Dv[flat] = D;
-        double* dqr = dq + flat * d;
-        for (long c = 0; c < d; ++c) dqr[c] = 0.0;
-        if (L[flat] <= 0.0) continue;
-        for (long j = 0; j < Sk; ++j) {
-          if (!is_visible(i, j, Sq, Sk, causal, ks, ke, km)) continue;
-          const double pij = exp(s[j] - M[flat]) / L[flat];
-          double dp = 0.0;
-          for (long c = 0; c < d; ++c) dp += dorow[c] * ld(vv, kvbase + j * d + c);
-          const double dsij = pij * (dp * drop_factor(&dr, b * Hq + h, i, j) - D);
-          for (long c = 0; c < d; ++c) dqr[c] += scale * dsij * ld(kk, kvbase + j * d + c);
-        }
-      }
+      for (long flat = 0; flat < nrow; ++flat)
+        dq_row(qs, kk, vv, dos, flat, B, Hq, Hkv, Sq, Sk, d, causal, scale, k_start, k_end,
+               key_mask, &dr, s, qrow, dorow, u, orow, dq + flat * d, &M[flat], &L[flat],
+               &Dv[flat]);
     }
     free(s);
     free(qrow);
@@ -456,6 +474,47 @@ done:
   free(M);
   free(L);
   free(Dv);
+  return err;
+}
+
+/*
+ * dQ of selected query rows only (rows: nrows flat row ids (b*Hq + h)*Sq + i;
+ * dq: [nrows, d]), each from its own statistics -- O(Sk * d) per row, so it
+ * serves problems too large for the full backward.
+ */
+int oracle_bwd_dq_rows(const void* q, const void* k, const void* v, const void* dout,
+                       int in_bf16, long B, long Hq, long Hkv, long Sq, long Sk, long d,
+                       int causal, double scale, const int* k_start, const int* k_end,
+                       const unsigned char* key_mask, double p_drop, unsigned long long seed,
+                       unsigned int offset, long nrows, const long* rows, double* dq) {
+  if (Hkv <= 0 || Hq % Hkv != 0) return 1;
+  const drop_t dr = make_drop(p_drop, seed, offset);
+  src_t qs = {q, in_bf16}, kk = {k, in_bf16}, vv = {v, in_bf16}, dos = {dout, in_bf16};
+  int err = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+    double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+    double* dorow = (double*)malloc(sizeof(double) * (size_t)d);
+    double* u = (double*)malloc(sizeof(double) * (size_t)d);
+    double* orow = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!s || !qrow || !dorow || !u || !orow) {
+#pragma omp atomic write
+      err = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (long r = 0; r < nrows; ++r) {
+        double m, l, D;
+        dq_row(qs, kk, vv, dos, rows[r], B, Hq, Hkv, Sq, Sk, d, causal, scale, k_start, k_end,
+               key_mask, &dr, s, qrow, dorow, u, orow, dq + r * d, &m, &l, &D);
+      }
+    }
+    free(s);
+    free(qrow);
+    free(dorow);
+    free(u);
+    free(orow);
+  }
   return err;
 }
 

@@ -55,6 +55,9 @@ def _load():
                                        D, P, P, P, D, U64, U32, P, P, P]
             lib.oracle_probs.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, L, ctypes.c_int,
                                          D, P, P, P, D, U64, U32, P, P]
+            lib.oracle_bwd_dq_rows.argtypes = [P, P, P, P, ctypes.c_int, L, L, L, L, L, L,
+                                               ctypes.c_int, D, P, P, P, D, U64, U32, L, P, P]
+            lib.oracle_bwd_dq_rows.restype = ctypes.c_int
             lib.oracle_philox4x32_10.argtypes = [P, U32, U32, P]
             lib.oracle_philox4x32_10.restype = None
             lib.oracle_dropout_keep.argtypes = [D, U64, U32, L, L, L]
@@ -195,6 +198,29 @@ def bwd(q, k, v, dout, causal: bool, scale: float, k_start=None, k_end=None, key
     if rc:
         raise RuntimeError(f"oracle_bwd failed ({rc})")
     return dq, dk, dv
+
+
+def bwd_dq_rows(q, k, v, dout, causal: bool, scale: float, rows, k_start=None, k_end=None,
+                key_mask=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
+    """dQ of selected query rows (flat ids (b*Hq + h)*Sq + i), each from its
+    own statistics by the same definition as bwd; returns [len(rows), d].
+    O(Sk * d) per row, for problems too large for the full backward."""
+    qa, bf = _as_input(q)
+    ka, _ = _as_input(k)
+    va, _ = _as_input(v)
+    da, _ = _as_input(dout)
+    B, Hq, Sq, d = qa.shape
+    _, Hkv, Sk, _ = ka.shape
+    rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    dq = np.empty((rr.shape[0], d), np.float64)
+    rc = _load().oracle_bwd_dq_rows(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), bf, B, Hq, Hkv, Sq,
+                                    Sk, d, int(causal), float(scale), _ptr(_i32(k_start, B)),
+                                    _ptr(_i32(k_end, B)), _ptr(_mask(key_mask, B, Sk)),
+                                    float(dropout_p), int(seed), int(offset), rr.shape[0],
+                                    _ptr(rr), _ptr(dq))
+    if rc:
+        raise RuntimeError(f"oracle_bwd_dq_rows failed ({rc})")
+    return dq
 
 
 def probs(q, k, v, causal: bool, scale: float, dout=None, k_start=None, k_end=None,

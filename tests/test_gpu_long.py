@@ -1,0 +1,65 @@
+"""Long sequences (the largest sizes of this suite): the forward and backward at
+S = 65536 and 131072 against the FP64 oracle on sampled rows, and dK/dV
+through identities that hold at any size:
+  sum over keys of dV_j = sum over query rows (that see a key) of dO_i,
+    because each row of P sums to 1;
+  sum over keys of dK_j = scale * sum_i q_i * (sum_j dS_ij) = 0,
+    because each row of dS sums to 0 (up to D_i taken from the bf16 O)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import io_aware_exact_tcgen05_gb300 as fa
+from io_aware_exact_tcgen05_gb300 import workloads
+from oracle import oracle as orc
+from tests.parity import check_grad, check_lse, check_o, sample_rows, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _must(S):
+    return [0, 1, 127, 128, 129, S // 2, S - 129, S - 128, S - 1]
+
+
+def test_forward_131072_sampled_rows():
+    B, Hq, Hkv, S, d = 1, 2, 1, 131072, 128
+    t = workloads.random_qkv(B, Hq, Hkv, S, S, d, seed=111)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fa_fwd(t["q"].to(DEV), t["k"].to(DEV), t["v"].to(DEV), True, scale)
+    torch.cuda.synchronize()
+    st, word = fa.fa_device_status()
+    assert st == 0, hex(word)
+    rows = sample_rows(B, Hq, S, 64, seed=112, must=_must(S) + [S + r for r in _must(S)])
+    ro, rl = orc.fwd(t["q"], t["k"], t["v"], True, scale, rows=rows)
+    check_o(to_np(o).reshape(-1, d)[rows], ro)
+    check_lse(to_np(lse).reshape(-1)[rows], rl)
+
+
+def test_backward_65536_sampled_rows_and_identities():
+    B, Hq, Hkv, S, d = 1, 2, 1, 65536, 128
+    t = workloads.random_qkv(B, Hq, Hkv, S, S, d, seed=113, with_dout=True)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = (t[n].to(DEV) for n in ("q", "k", "v", "dout"))
+    o, lse = fa.fa_fwd(q, k, v, True, scale)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, do, lse, True, scale)
+    torch.cuda.synchronize()
+    st, word = fa.fa_device_status()
+    assert st == 0, hex(word)
+    rows = sample_rows(B, Hq, S, 24, seed=114, must=_must(S) + [S + 1, 2 * S - 1])
+    ro, rl = orc.fwd(t["q"], t["k"], t["v"], True, scale, rows=rows)
+    check_o(to_np(o).reshape(-1, d)[rows], ro)
+    check_lse(to_np(lse).reshape(-1)[rows], rl)
+    rq = orc.bwd_dq_rows(t["q"], t["k"], t["v"], t["dout"], True, scale, rows)
+    check_grad(to_np(dq).reshape(-1, d)[rows], rq, "dQ rows")
+    # identities over all keys of the KV head (both query heads read it)
+    dv_sum = to_np(dv)[0, 0].sum(axis=0)
+    do_sum = to_np(do)[0].sum(axis=(0, 1))  # every causal row sees key 0
+    dv_abs = np.abs(to_np(dv)[0, 0]).sum(axis=0)
+    assert np.all(np.abs(dv_sum - do_sum) <= 1e-2 * dv_abs + 1e-2), \
+        float(np.abs(dv_sum - do_sum).max())
+    dk_sum = to_np(dk)[0, 0].sum(axis=0)
+    dk_abs = np.abs(to_np(dk)[0, 0]).sum(axis=0)
+    assert np.all(np.abs(dk_sum) <= 2e-2 * dk_abs), float((np.abs(dk_sum) / dk_abs).max())

@@ -559,6 +559,19 @@ def test_bf16_inputs_widen_exactly():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+def test_dq_rows_equal_full_backward():
+    B, Hq, Hkv, S, d = 2, 4, 2, 37, 16
+    q = _rand((B, Hq, S, d), 100)
+    k = _rand((B, Hkv, S, d), 101)
+    v = _rand((B, Hkv, S, d), 102)
+    do = _rand((B, Hq, S, d), 103)
+    for causal in (False, True):
+        dq, _, _ = orc.bwd(q, k, v, do, causal, 0.3, k_start=[3, 0], k_end=[37, 20])
+        rows = [0, 5, 36, 37, 80, 143, B * Hq * S - 1]
+        got = orc.bwd_dq_rows(q, k, v, do, causal, 0.3, rows, k_start=[3, 0], k_end=[37, 20])
+        assert np.array_equal(got, dq.reshape(-1, d)[rows])
+
+
 def test_row_subset_equals_full():
     q = _rand((2, 4, 20, 8), 95)
     k = _rand((2, 2, 20, 8), 96)
