@@ -222,14 +222,15 @@ fa_status check_key_bits(const uint32_t* bits) {
 }
 
 // Dropout arguments from the caller's probability, seed and offset: keep a
-// weight iff its Philox word is >= floor(p * 2^32) (computed in double, the
-// same integer threshold the reference computation uses).
+// weight iff its 16-bit Philox draw is >= floor(p * 2^16) (computed in
+// double, the same integer threshold the reference computation uses).
 fa_status make_dropout(float p_drop, unsigned long long seed, unsigned int offset,
                        fa::DropoutArgs* out) {
   if (!(p_drop >= 0.f && p_drop < 1.f))
     return fail(FA_ERR_INVALID_ARG, "dropout_p (%g) must lie in [0, 1)", (double)p_drop);
   fa::DropoutArgs dr{};
-  dr.thr = static_cast<uint32_t>(std::floor(static_cast<double>(p_drop) * 4294967296.0));
+  dr.thr_hi = static_cast<uint32_t>(std::floor(static_cast<double>(p_drop) * 65536.0)) << 16;
+  dr.on = p_drop > 0.f ? 1u : 0u;
   dr.seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
   dr.seed_hi = static_cast<uint32_t>(seed >> 32);
   dr.offset = offset;
@@ -238,7 +239,7 @@ fa_status make_dropout(float p_drop, unsigned long long seed, unsigned int offse
   return FA_OK;
 }
 
-const fa::DropoutArgs kNoDropout{0u, 0u, 0u, 0u, 1.f};
+const fa::DropoutArgs kNoDropout{0u, 0u, 0u, 0u, 1.f, 0u};
 
 fa_status fwd_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,

@@ -412,11 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(grp * 32) << 16;
     const float c = p.scale_log2;
     const uint32_t ds_base = smem_u32(s.ds[0]);
-    // dropout: the four lanes of keys 4a..4a+3 share a Philox counter per
-    // query (the key tile starts on a multiple of 4 keys); lane (l & 3) of the
-    // group draws query t = l & 3 of each block of 4 and ballots hand every
-    // lane its own key's bits
-    const uint32_t grp4 = static_cast<uint32_t>(lane & ~3);
+    // dropout: the eight lanes of keys 8a..8a+7 share a Philox counter per
+    // query (the key tile starts on a multiple of 8 keys); lane (l & 7) of the
+    // group draws query t = l & 7 of each block of 8, and eight ballots (one
+    // per key of the group) hand every lane its own key's bits
+    const uint32_t grp8 = static_cast<uint32_t>(lane & ~7);
+    const uint32_t kix = static_cast<uint32_t>(lane & 7);  // this lane's key in its group
     int ig = 0, uk = 0;  // iterations and units with work, across the CTA's units
     bool ok = true;
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t w = __ldg(p.key_bits + static_cast<size_t>(bz) * p.mask_words + key / 32);
         key_in = (w >> (key & 31)) & 1u;
       }
-      const uint32_t key4 = static_cast<uint32_t>(key) >> 2;
+      const uint32_t key8 = static_cast<uint32_t>(key) >> 3;
       for (int it = 0; it < n_it; ++it) {
         const int gi = ig + it;  // this iteration's index across units (barrier phases)
         const int g = it / n_qt;
@@ -479,16 +480,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bh = static_cast<uint32_t>(bz * p.Hq + h);
             uint32_t kw = 0;
 #pragma unroll
-            for (int g4 = 0; g4 < 8; ++g4) {
-              const uint32_t qi = static_cast<uint32_t>(q0 + hf * 64 + cc * 32 + g4 * 4) +
-                                  static_cast<uint32_t>(lane & 3);
-              const uint32_t k4 = dropout_keep4(p.drop, key4, qi, bh);
-              const uint32_t b0 = __ballot_sync(0xffffffffu, k4 & 1u);
-              const uint32_t b1 = __ballot_sync(0xffffffffu, k4 & 2u);
-              const uint32_t b2 = __ballot_sync(0xffffffffu, k4 & 4u);
-              const uint32_t b3 = __ballot_sync(0xffffffffu, k4 & 8u);
-              const uint32_t sel = (lane & 2) ? ((lane & 1) ? b3 : b2) : ((lane & 1) ? b1 : b0);
-              kw |= ((sel >> grp4) & 0xFu) << (4 * g4);
+            for (int g8 = 0; g8 < 4; ++g8) {
+              const uint32_t qi = static_cast<uint32_t>(q0 + hf * 64 + cc * 32 + g8 * 8) + kix;
+              const uint32_t k8 = dropout_keep8(p.drop, key8, qi, bh);
+              // bit L of bt[t]: key 8 (L / 8) + t kept for the query lane L drew
+              uint32_t bt[8];
+#pragma unroll
+              for (int t = 0; t < 8; ++t) bt[t] = __ballot_sync(0xffffffffu, (k8 >> t) & 1u);
+              const uint32_t s0 = (kix & 1) ? bt[1] : bt[0];
+              const uint32_t s1 = (kix & 1) ? bt[3] : bt[2];
+              const uint32_t s2 = (kix & 1) ? bt[5] : bt[4];
+              const uint32_t s3 = (kix & 1) ? bt[7] : bt[6];
+              const uint32_t sel = (kix & 4) ? ((kix & 2) ? s3 : s2) : ((kix & 2) ? s1 : s0);
+              kw |= ((sel >> grp8) & 0xFFu) << (8 * g8);
             }
             keepw[cc] = kw;
           }
@@ -690,7 +694,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   constexpr size_t smem = sizeof(BwdSmem<D>);
   static_assert(smem <= 232448, "backward shared memory exceeds the per-CTA limit");
   static bool configured[2] = {false, false};
-  const bool drop = p.drop.thr != 0;
+  const bool drop = p.drop.on != 0;
   if (!configured[drop]) {
     cudaError_t e = cudaFuncSetAttribute(drop ? fa_bwd_main<D, true> : fa_bwd_main<D, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

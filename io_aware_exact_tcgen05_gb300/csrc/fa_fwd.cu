@@ -116,15 +116,15 @@ __device__ __forceinline__ void mask_key_bits(uint32_t (&sr)[kTileN], uint4 kb) 
 // from t_p.  sum2 gathers the fp32 weights (for l); sr_lo/sr_hi gather the
 // rounded ones (for lr).  With DROP, the stored words of dropped weights are
 // cleared after the sums (l, lr and the LSE stay those of the undropped
-// softmax); key4 is the tile's first key / 4, row and bh the Philox counter's
+// softmax); key8 is the tile's first key / 8, row and bh the Philox counter's
 // query row and query head.
 template <int HALF, bool DROP>
 __device__ __forceinline__ void softmax_half(const uint32_t (&sr)[kTileN], uint64_t c2,
                                              uint64_t nmc2, uint32_t t_p, uint64_t (&sum2)[4],
                                              float (&sr_lo)[4], float (&sr_hi)[4],
-                                             const DropoutArgs& drop, uint32_t key4, uint32_t row,
+                                             const DropoutArgs& drop, uint32_t key8, uint32_t row,
                                              uint32_t bh) {
-  uint32_t keep4 = 0;
+  uint32_t keep8 = 0;
   uint32_t pk[kTileN / 4];
 #pragma unroll
   for (int jq = 0; jq < kTileN / 4; ++jq) {
@@ -139,8 +139,8 @@ __device__ __forceinline__ void softmax_half(const uint32_t (&sr)[kTileN], uint6
     sum2[jq & 3] = f2_add(sum2[jq & 3], f2_pack(p0, p1));
     add_bf16x2_f32(sr_lo[jq & 3], sr_hi[jq & 3], pk[jq]);
     if (DROP) {
-      if ((jq & 1) == 0) keep4 = dropout_keep4(drop, key4 + HALF * 16 + jq / 2, row, bh);
-      const uint32_t kb = keep4 >> (2 * (jq & 1));
+      if ((jq & 3) == 0) keep8 = dropout_keep8(drop, key8 + HALF * 8 + jq / 4, row, bh);
+      const uint32_t kb = keep8 >> (2 * (jq & 3));
       pk[jq] &= ((kb & 1u) ? 0x0000ffffu : 0u) | ((kb & 2u) ? 0xffff0000u : 0u);
     }
   }
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
         tmem_wait_ld();
         const int c0 = (j0 + j) * kTileN;
-        const uint32_t key4 = static_cast<uint32_t>(c0) >> 2;  // dropout counter word 0
+        const uint32_t key8 = static_cast<uint32_t>(c0) >> 3;  // dropout counter word 0
         const bool need_mask = (c0 < klo) || (c0 + kTileN > khi_row);
         const bool masked_tile = __any_sync(0xffffffffu, need_mask);
         if (masked_tile) mask_scores<0, kTileN>(sr, c0, klo, khi_row);
@@ -480,8 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!exact) {
           const float mc = m * c;
           const uint64_t nmc2 = f2_pack(-mc, -mc);
-          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key4, i, bh);
-          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key4, i, bh);
+          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key8, i, bh);
+          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key8, i, bh);
           const float ts = sum_f2x4(sum2);
           exact = __any_sync(0xffffffffu, !(ts < kFastLimit));
           if (!exact) {
@@ -535,8 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             sr_lo[q2] = 0.f;
             sr_hi[q2] = 0.f;
           }
-          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key4, i, bh);
-          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key4, i, bh);
+          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key8, i, bh);
+          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key8, i, bh);
           l += sum_f2x4(sum2);
           lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
                 ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
@@ -650,7 +650,7 @@ cudaError_t launch_fwd_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 template <int D>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdParams& p, cudaStream_t stream) {
-  if (p.drop.thr != 0) return launch_fwd_dd<D, kModeDropout>(tq, tk, tv, p, stream);
+  if (p.drop.on) return launch_fwd_dd<D, kModeDropout>(tq, tk, tv, p, stream);
   if (p.key_bits) return launch_fwd_dd<D, kModeKeyBits>(tq, tk, tv, p, stream);
   return launch_fwd_dd<D, kModePlain>(tq, tk, tv, p, stream);
 }

@@ -33,11 +33,12 @@ constexpr int kTileN = 128;
 
 // Dropout on the attention weights (see fa_philox.cuh for the mapping).
 struct DropoutArgs {
-  uint32_t thr;      // floor(p * 2^32); 0 = dropout off
+  uint32_t thr_hi;   // floor(p * 2^16) << 16: the 16-bit threshold in the high half
   uint32_t seed_lo;
   uint32_t seed_hi;
   uint32_t offset;
   float scale;       // 1 / (1 - p)
+  uint32_t on;       // p > 0
 };
 
 struct FwdParams {
@@ -54,7 +55,7 @@ struct FwdParams {
   // row = batch row (or 0 for packed keys); nullptr = every key visible.
   const uint32_t* key_bits;
   int mask_words;
-  DropoutArgs drop;    // thr == 0: no dropout
+  DropoutArgs drop;    // on == 0: no dropout
   int B, Hq, Hkv, Sq, Sk;
   int group;           // Hq / Hkv
   int pack_heads;      // 1: a CTA's two query tiles are two heads of one KV group
@@ -131,7 +132,7 @@ struct BwdParams {
   const int32_t* cu_k;
   const uint32_t* key_bits;  // optional key visibility bits, as in FwdParams
   int mask_words;
-  DropoutArgs drop;          // the forward's dropout (thr == 0: none)
+  DropoutArgs drop;          // the forward's dropout (on == 0: none)
   int grid_b;  // units along the grid's batch axis: B, or the sequence count when packed
   int n_kt;    // key tiles per unit: ceil(Sk / 128), or ceil(longest sequence's keys / 128)
   int B, Hq, Hkv, Sq, Sk, group;

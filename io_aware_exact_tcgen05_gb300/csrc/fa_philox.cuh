@@ -11,8 +11,10 @@
 // Dropout mapping (part of the forward/backward contract, FlashAttention_01
 // page, "why the backward can recompute" and "interface and implementation
 // constraints"): weight (query row i, key j) of query head bh = b * Hq + h
-// is kept iff word (j mod 4) of Philox4x32-10 at counter
-// (j / 4, i, bh, offset) under key (seed low, seed high) is >= floor(p * 2^32).
+// is kept iff half (j mod 2) (0: low 16 bits, 1: high 16 bits) of word
+// ((j mod 8) / 2) of Philox4x32-10 at counter (j / 8, i, bh, offset) under
+// key (seed low, seed high) is >= floor(p * 2^16).  One call decides eight
+// keys.
 #pragma once
 
 #include <cstdint>
@@ -40,12 +42,18 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Keep bits of keys 4*j4 .. 4*j4+3 at query row i of head bh (bit t = key 4*j4+t).
-__device__ __forceinline__ uint32_t dropout_keep4(const DropoutArgs& d, uint32_t j4, uint32_t i,
+// Keep bits of keys 8*j8 .. 8*j8+7 at query row i of head bh (bit t = key
+// 8*j8+t).  A high half is >= the threshold iff the whole word is >= thr_hi;
+// a low half iff the word shifted up by 16 is.
+__device__ __forceinline__ uint32_t half_keep2(uint32_t w, uint32_t thr_hi) {
+  return ((w << 16) >= thr_hi ? 1u : 0u) | (w >= thr_hi ? 2u : 0u);
+}
+
+__device__ __forceinline__ uint32_t dropout_keep8(const DropoutArgs& d, uint32_t j8, uint32_t i,
                                                   uint32_t bh) {
-  const uint4 w = philox4x32_10(make_uint4(j4, i, bh, d.offset), d.seed_lo, d.seed_hi);
-  return (w.x >= d.thr ? 1u : 0u) | (w.y >= d.thr ? 2u : 0u) | (w.z >= d.thr ? 4u : 0u) |
-         (w.w >= d.thr ? 8u : 0u);
+  const uint4 w = philox4x32_10(make_uint4(j8, i, bh, d.offset), d.seed_lo, d.seed_hi);
+  return half_keep2(w.x, d.thr_hi) | (half_keep2(w.y, d.thr_hi) << 2) |
+         (half_keep2(w.z, d.thr_hi) << 4) | (half_keep2(w.w, d.thr_hi) << 6);
 }
 
 }  // namespace fa

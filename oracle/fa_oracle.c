@@ -47,8 +47,9 @@
  *   dP_ij = keep_ij / (1 - p) <dO_i, v_j>,  dV_j = sum_i p_ij keep_ij / (1 - p) dO_i
  * keep_ij comes from Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel
  * random numbers: as easy as 1, 2, 3", SC 2011) with counter
- * (j / 4, i, b * Hq + h, offset) and key (seed low word, seed high word):
- * keep_ij <=> word (j mod 4) >= floor(p * 2^32).
+ * (j / 8, i, b * Hq + h, offset) and key (seed low word, seed high word):
+ * keep_ij <=> the 16-bit half (j mod 2) (0: low, 1: high) of word
+ * ((j mod 8) / 2) is >= floor(p * 2^16).
  *
  * Inputs are either fp64 arrays or bf16 bit patterns (uint16); a bf16 value
  * is widened to fp64 exactly.  Layout is [B, H, S, d], d innermost.
@@ -113,7 +114,7 @@ void oracle_philox4x32_10(const uint32_t* ctr, uint32_t k0, uint32_t k1, uint32_
 
 typedef struct {
   int on;
-  uint32_t thr;          /* floor(p * 2^32): keep iff the word is >= thr */
+  uint32_t thr;          /* floor(p * 2^16): keep iff the 16-bit draw is >= thr */
   double keep_scale;     /* 1 / (1 - p) */
   uint32_t seed_lo, seed_hi, offset;
 } drop_t;
@@ -121,7 +122,7 @@ typedef struct {
 static drop_t make_drop(double p, unsigned long long seed, unsigned int offset) {
   drop_t d;
   d.on = p > 0.0;
-  d.thr = d.on ? (uint32_t)floor(p * 4294967296.0) : 0u;
+  d.thr = d.on ? (uint32_t)floor(p * 65536.0) : 0u;
   d.keep_scale = d.on ? 1.0 / (1.0 - p) : 1.0;
   d.seed_lo = (uint32_t)(seed & 0xffffffffull);
   d.seed_hi = (uint32_t)(seed >> 32);
@@ -132,10 +133,12 @@ static drop_t make_drop(double p, unsigned long long seed, unsigned int offset) 
 /* keep_ij / (1 - p) for query row i of query head bh (= b * Hq + h), key j */
 static double drop_factor(const drop_t* d, long bh, long i, long j) {
   if (!d || !d->on) return 1.0;
-  const uint32_t ctr[4] = {(uint32_t)(j >> 2), (uint32_t)i, (uint32_t)bh, d->offset};
+  const uint32_t ctr[4] = {(uint32_t)(j / 8), (uint32_t)i, (uint32_t)bh, d->offset};
   uint32_t w[4];
   philox4x32_10(ctr, d->seed_lo, d->seed_hi, w);
-  return (w[j & 3] >= d->thr) ? d->keep_scale : 0.0;
+  const uint32_t word = w[(j % 8) / 2];
+  const uint32_t draw = (j % 2) ? (word >> 16) : (word & 0xffffu);
+  return (draw >= d->thr) ? d->keep_scale : 0.0;
 }
 
 /* 1 when weight (i, j) of query head bh is kept, 0 when dropped */

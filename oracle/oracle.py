@@ -255,8 +255,9 @@ def philox4x32_10(counter, key):
 
 def dropout_keep(p: float, seed: int, offset: int, bh: int, i: int, j: int) -> bool:
     """Whether weight (query row i, key j) of query head bh = b*Hq + h is kept:
-    word j % 4 of Philox4x32-10 at counter (j // 4, i, bh, offset) under key
-    (seed low 32 bits, seed high 32 bits) is >= floor(p * 2^32)."""
+    the 16-bit half j % 2 (0: low, 1: high) of word (j % 8) // 2 of
+    Philox4x32-10 at counter (j // 8, i, bh, offset) under key (seed low 32
+    bits, seed high 32 bits) is >= floor(p * 2^16)."""
     return bool(_load().oracle_dropout_keep(float(p), int(seed), int(offset), bh, i, j))
 
 

@@ -1,8 +1,9 @@
 """GPU dropout (fa_fwd_dropout / fa_bwd_dropout through the C ABI) against the
 FP64 oracle's Philox4x32-10 mapping: the keep decisions must agree exactly
-(they are integer comparisons on both sides), and O, LSE, dQ, dK, dV within
-the usual tolerances.  Probabilities are exact in float32, so both sides use
-the same integer threshold."""
+(they are integer comparisons of 16-bit draws on both sides), and O, LSE, dQ,
+dK, dV within the usual tolerances.  Probabilities are exact in float32, so
+both sides use the same integer threshold; 2^-17 has threshold 0 (every
+weight kept, and still scaled by 1 / (1 - p))."""
 import math
 
 import numpy as np
@@ -23,7 +24,7 @@ def _status_ok():
     assert st == 0, hex(word)
 
 
-@pytest.mark.parametrize("p", [0.25, 0.625])
+@pytest.mark.parametrize("p", [0.25, 0.625, 2.0**-17])
 def test_keep_decisions_match_the_mapping_exactly(p):
     # scale 0: every visible key has weight 1/128; V row j is the unit vector
     # e_(j - k0), so O[..., c] = keep(key k0 + c) / (1 - p) / 128 reads the

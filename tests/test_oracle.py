@@ -354,10 +354,21 @@ def test_dropout_keep_rate_and_mapping():
     n = keep.size
     sigma = math.sqrt(n * p * (1 - p))
     assert abs(keep.sum() - n * (1 - p)) < 5 * sigma
-    # the decision is word j % 4 of the Philox call at counter (j // 4, i, bh, offset)
-    for (bh, i, j) in [(0, 0, 0), (1, 5, 6), (1, 59, 255), (0, 17, 3)]:
-        w = orc.philox4x32_10([j // 4, i, bh, off], [seed & 0xffffffff, seed >> 32])
-        assert orc.dropout_keep(p, seed, off, bh, i, j) == (int(w[j % 4]) >= int(p * 2**32))
+    # the decision is the 16-bit half j % 2 of word (j % 8) // 2 of the Philox
+    # call at counter (j // 8, i, bh, offset), against floor(p * 2^16)
+    for (bh, i, j) in [(0, 0, 0), (1, 5, 6), (1, 59, 255), (0, 17, 3), (1, 2, 7), (0, 44, 9)]:
+        w = orc.philox4x32_10([j // 8, i, bh, off], [seed & 0xffffffff, seed >> 32])
+        draw = (int(w[(j % 8) // 2]) >> (16 * (j % 2))) & 0xFFFF
+        assert orc.dropout_keep(p, seed, off, bh, i, j) == (draw >= int(p * 2**16))
+    # eight consecutive keys share one call; the next eight use the next counter
+    w0 = orc.philox4x32_10([0, 3, 1, off], [seed & 0xffffffff, seed >> 32])
+    w1 = orc.philox4x32_10([1, 3, 1, off], [seed & 0xffffffff, seed >> 32])
+    halves = [(int(x) >> s) & 0xFFFF for w in (w0, w1) for x in w for s in (0, 16)]
+    assert [orc.dropout_keep(p, seed, off, 1, 3, j) for j in range(16)] == \
+        [h >= int(p * 2**16) for h in halves]
+    # a probability below 2^-16 keeps every weight (its kept weights are still
+    # scaled by 1 / (1 - p))
+    assert all(orc.dropout_keep(1e-6, seed, off, 0, 3, j) for j in range(64))
     # p = 0 keeps everything; another seed or offset gives another mask
     assert all(orc.dropout_keep(0.0, seed, off, 0, 3, j) for j in range(64))
     a = [orc.dropout_keep(p, seed, off, 0, 3, j) for j in range(256)]
