@@ -19,7 +19,8 @@
 // scale * q_descale * k_descale, and O is multiplied by v_descale once in the
 // epilogue.  Weights are kept below 448 (e4m3's largest finite value): the
 // fast path accepts a tile only while the row's fp32 weight sum stays below
-// it, and the exact path rescales once the max grows by more than 2^8.  O is
+// it, and the exact path rescales once the max grows by more than 2^1, so
+// that later tiles of the row pass that bound again.  O is
 // divided by the sum of the *rounded* weights (what the PV product used), l
 // (fp32, unrounded) gives the LSE.
 //

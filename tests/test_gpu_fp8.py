@@ -36,12 +36,12 @@ def _quant(x):
     return (xf / ds).to(F8), ds
 
 
-def _case(B, Hq, Hkv, Sq, Sk, causal, seed, ks=None, ke=None):
+def _case(B, Hq, Hkv, Sq, Sk, causal, seed, ks=None, ke=None, qmul=1.0):
     if F8 is None:
         pytest.skip("torch without float8_e4m3fn")
     d = 128
     t = workloads.random_qkv(B, Hq, Hkv, Sq, Sk, d, seed=seed)
-    q8, qd = _quant(t["q"])
+    q8, qd = _quant(t["q"].float() * qmul)
     k8, kd = _quant(t["k"])
     v8, vd = _quant(t["v"])
     vt8 = v8.transpose(-1, -2).contiguous()
@@ -84,6 +84,13 @@ def _case(B, Hq, Hkv, Sq, Sk, causal, seed, ks=None, ke=None):
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_forward_within_rounding_bound(causal):
     _case(1, 4, 2, 384, 384, causal, seed=81)
+
+
+def test_fp8_forward_large_logits_max_growth():
+    # Q x 8: raw logits reach about +-100, so a row's max keeps growing across
+    # key tiles and the redo path (and its rescale threshold) runs repeatedly
+    _case(1, 2, 2, 512, 1024, True, seed=84, qmul=8.0)
+    _case(1, 2, 1, 300, 304, False, seed=85, qmul=8.0)
 
 
 def test_fp8_forward_rectangular_interval_and_slots():
