@@ -577,15 +577,8 @@ def next_rows_bench(fa, dev, peaks, w, q, k, v, do, kst, ken, o, lse, dq, dk, dv
                      "bwd_tflops": 2.5 * f_vf / ms_b / 1e9,
                      "bwd_frac": 2.5 * f_vf / ms_b / 1e9 / peak_t}
     # FP8 (e4m3) forward on the same shapes; per-tensor descale = max|x| / 448
-    f8 = getattr(torch, "float8_e4m3fn", None)
-    if f8 is not None:
-        def quant(x):
-            ds = float(x.float().abs().max()) / 448.0
-            return (x.float() / ds).to(f8), ds
-        q8, qd = quant(q)
-        k8, kd = quant(k)
-        v8, vd = quant(v)
-        vt8 = v8.transpose(-1, -2).contiguous()
+    if getattr(torch, "float8_e4m3fn", None) is not None:
+        q8, qd, k8, kd, vt8, vd = _fp8_inputs(q, k, v)
         peak8 = 2.0 * peak_t  # the nominal FP8 : BF16 dense ratio (4.5 : 2.25 PFLOP/s)
         ms_f = timed(lambda: fa.fa_fwd_fp8(q8, k8, vt8, True, w.scale, qd, kd, vd, k_start=kst,
                                            k_end=ken, o=o, lse=lse))
@@ -596,6 +589,19 @@ def next_rows_bench(fa, dev, peaks, w, q, k, v, do, kst, ken, o, lse, dq, dk, dv
     if st != 0:
         raise RuntimeError(f"device status after the widened rows: {word:#x}")
     return out
+
+
+def _fp8_inputs(q, k, v):
+    """e4m3 Q, K and V^T ([B, Hkv, d, Sk]) with per-tensor descales max|x| / 448."""
+    f8 = torch.float8_e4m3fn
+
+    def quant(x):
+        ds = float(x.float().abs().max()) / 448.0
+        return (x.float() / ds).to(f8), ds
+    q8, qd = quant(q)
+    k8, kd = quant(k)
+    v8, vd = quant(v)
+    return q8, qd, k8, kd, v8.transpose(-1, -2).contiguous(), vd
 
 
 def decode_bench(fa, dev, peaks, args, ws):
@@ -646,9 +652,10 @@ def decode_bench(fa, dev, peaks, args, ws):
 
 
 def run_only(args):
-    """Profiling aid: run just one call kind of the step (fwd, bwd or decode)
-    `--warmup` + `--steps` times on the same workload, no timing JSON.  Used as
-    the command an ncu capture of a single kernel runs."""
+    """Profiling aid: run just one call kind (fwd, bwd, decode, the FP8
+    forward or the dropout forward at p = 0.1 on the step's workload)
+    `--warmup` + `--steps` times, no timing JSON.  Used as the command an ncu
+    capture of a single kernel runs."""
     import io_aware_exact_tcgen05_gb300 as fa
     fa.load_library()
     dev = torch.device("cuda", 0)
@@ -659,6 +666,14 @@ def run_only(args):
         q, kc, vc, sl = (t[x].to(dev) for x in ("q", "k", "v", "seqlens_k"))
         for _ in range(n):
             fa.fa_decode(q, kc, vc, sl, w.scale)
+    elif args.only == "fp8":
+        w = workloads.make(WORKLOAD)
+        t = w.tensors
+        q, k, v = (t[x].to(dev) for x in ("q", "k", "v"))
+        kst, ken = t["k_start"].to(dev), t["k_end"].to(dev)
+        q8, qd, k8, kd, vt8, vd = _fp8_inputs(q, k, v)
+        for _ in range(n):
+            fa.fa_fwd_fp8(q8, k8, vt8, True, w.scale, qd, kd, vd, k_start=kst, k_end=ken)
     else:
         w = workloads.make(WORKLOAD)
         t = w.tensors
@@ -668,6 +683,9 @@ def run_only(args):
         for _ in range(n):
             if args.only == "fwd":
                 fa.fa_fwd(q, k, v, True, w.scale, k_start=kst, k_end=ken, o=o, lse=lse)
+            elif args.only == "fwd_dropout":
+                fa.fa_fwd(q, k, v, True, w.scale, k_start=kst, k_end=ken, o=o, lse=lse,
+                          dropout_p=0.1, seed=1, offset=0)
             else:
                 fa.fa_bwd(q, k, v, o, do, lse, True, w.scale, k_start=kst, k_end=ken)
     st, word = fa.fa_device_status()
@@ -686,7 +704,7 @@ def main():
     ap.add_argument("--skip-next", action="store_true",
                     help="skip the key-mask / dropout / varlen measurements")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--only", choices=["fwd", "bwd", "decode"], default=None)
+    ap.add_argument("--only", choices=["fwd", "bwd", "decode", "fp8", "fwd_dropout"], default=None)
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="with --only decode: fewer sequences (a smaller profiling case)")
     args = ap.parse_args()
