@@ -281,13 +281,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < un.n_it; ++it, ++ig) {
           const int st = ig % kQStages;
           const int use = ig / kQStages;
+          const int g = it / un.n_qt;
+          const int q0 = (un.qt_lo + it % un.n_qt) * kTileM;
+          const int zq = un.bz * p.Hq + un.hk * p.group + g;
+          // The stage frees only once the dQ reduce staged in it has been
+          // read (about a tile's time): meanwhile pull this tile's Q and dO
+          // into L2, so that the load below does not wait on DRAM.
+          for (int cb = 0; cb < NB; ++cb) {
+            tma_prefetch_l2_3d(&tq, cb * 64, un.qb + q0, zq);
+            tma_prefetch_l2_3d(&tdo, cb * 64, un.qb + q0, zq);
+          }
           if (use > 0 && !mbar_wait(&s.q_empty[st], (use - 1) & 1, abort_flag, kSiteQEmpty)) {
             ok = false;
             break;
           }
-          const int g = it / un.n_qt;
-          const int q0 = (un.qt_lo + it % un.n_qt) * kTileM;
-          const int zq = un.bz * p.Hq + un.hk * p.group + g;
           mbar_arrive_expect_tx(&s.q_full[st], 2 * NB * kBoxBytes);
           for (int cb = 0; cb < NB; ++cb) {
             tma_load_3d(s.q[st][cb], &tq, &s.q_full[st], cb * 64, un.qb + q0, zq);

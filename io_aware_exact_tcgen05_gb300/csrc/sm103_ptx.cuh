@@ -166,6 +166,15 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// Hint: bring a 3-D tile of global memory into L2 ahead of a later TMA load
+// of the same box (no shared memory, nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // 3-D tiled reduce-add of a shared-memory box into global memory (bulk
 // async-group completion).  Elements past the tensor's bounds are skipped.
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
