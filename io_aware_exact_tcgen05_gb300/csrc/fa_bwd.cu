@@ -111,8 +111,16 @@ struct BwdUnit {
 
 __device__ __forceinline__ BwdUnit bwd_unit_at(const BwdParams& p, int U) {
   BwdUnit u;
-  const int bh = U % (p.grid_b * p.Hkv);
-  const int kt = U / (p.grid_b * p.Hkv);
+  // Units run key-tile-major (heavy causal key tiles first) inside groups of
+  // unit_group (batch or sequence, KV head) pairs, group after group.
+  const int BH = p.grid_b * p.Hkv;
+  const int per_group = p.n_kt * p.unit_group;
+  const int grp = U / per_group;
+  const int first = grp * p.unit_group;
+  const int cnt = min(p.unit_group, BH - first);
+  const int r = U - grp * per_group;
+  const int kt = r / cnt;
+  const int bh = first + r % cnt;
   u.b = bh / p.Hkv;
   u.hk = bh % p.Hkv;
   u.sq = p.Sq;
@@ -721,12 +729,44 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>(p.n_kt) * p.grid_b * p.Hkv;
   const unsigned int grid = static_cast<unsigned int>(std::min<long long>(units, n_sm));
+  // Pairs per group.  A pair's dQ accumulators and Q/dO tiles take 8 bytes
+  // per row and head-dim column of each of its query heads.  While all pairs
+  // together stay within about twice L2 they form one group (the plain
+  // key-tile-major walk, best balanced).  Beyond that L2 thrashes: a group
+  // then holds about half of L2's worth of pairs, but at least three waves of
+  // units so the walk's pairing of heavy and light units stays balanced, and
+  // it is rounded to whole batch rows (or to a divisor of the KV heads), so
+  // that the units of a group share one sequence length.
+  BwdParams pu = p;
+  {
+    const long long pairs = static_cast<long long>(p.grid_b) * p.Hkv;
+    const long long rows = p.cu_q ? static_cast<long long>(p.n_kt) * kTileN : p.Sq;
+    const long long per_pair = std::max(1LL, 8LL * rows * D * p.group);
+    long long g = pairs;
+    if (pairs * per_pair > (256LL << 20)) {
+      const long long fit = std::max(1LL, (64LL << 20) / per_pair);
+      const long long waves = (3LL * n_sm + p.n_kt - 1) / std::max(1, p.n_kt);
+      const long long t = std::max(fit, waves);
+      if (t >= p.Hkv) {
+        g = static_cast<long long>(p.Hkv) * ((t + p.Hkv / 2) / p.Hkv);
+      } else {
+        g = 1;
+        for (long long dv = t; dv >= 1; --dv)
+          if (p.Hkv % dv == 0) {
+            g = dv;
+            break;
+          }
+      }
+      g = std::min(pairs, std::max(1LL, g));
+    }
+    pu.unit_group = static_cast<int>(g);
+  }
   if (grid > 0) {  // packed sequences that all lack keys: dQ stays zero
     hook_before(stream);
     if (drop)
-      fa_bwd_main<D, true><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, p);
+      fa_bwd_main<D, true><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, pu);
     else
-      fa_bwd_main<D, false><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, p);
+      fa_bwd_main<D, false><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, pu);
     hook_after(stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -135,6 +135,7 @@ struct BwdParams {
   DropoutArgs drop;          // the forward's dropout (on == 0: none)
   int grid_b;  // units along the grid's batch axis: B, or the sequence count when packed
   int n_kt;    // key tiles per unit: ceil(Sk / 128), or ceil(longest sequence's keys / 128)
+  int unit_group;  // (batch or sequence, KV head) pairs walked together (set by the launcher)
   int B, Hq, Hkv, Sq, Sk, group;
   int causal;
   float scale;
