@@ -743,7 +743,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     const long long rows = p.cu_q ? static_cast<long long>(p.n_kt) * kTileN : p.Sq;
     const long long per_pair = std::max(1LL, 8LL * rows * D * p.group);
     long long g = pairs;
-    if (pairs * per_pair > (256LL << 20)) {
+    if (per_pair > (256LL << 20) / std::max(1LL, pairs)) {  // pairs * per_pair, without overflow
       const long long fit = std::max(1LL, (64LL << 20) / per_pair);
       const long long waves = (3LL * n_sm + p.n_kt - 1) / std::max(1, p.n_kt);
       const long long t = std::max(fit, waves);
