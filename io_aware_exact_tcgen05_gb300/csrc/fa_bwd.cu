@@ -1,8 +1,8 @@
 // fa_bwd.cu -- backward attention by recomputation for sm_103a.
 //
 //   1. fa_bwd_pre:   D_i = rowsum(dO_i * O_i) (fp32) and dQacc = 0
-//   2. fa_bwd_main:  one CTA per (128-key tile, KV head, batch row).  K and V
-//                    stay in shared memory; the CTA walks every query head of
+//   2. fa_bwd_main:  work units of (128-key tile, KV head, batch row).  K and
+//                    V stay in shared memory; a unit walks every query head of
 //                    the group and every 128-row query tile that can see its
 //                    keys.  Per query tile (all five contractions on tcgen05):
 //        S^T  = K Q^T            (keys x queries, fp32 in TMEM)
@@ -31,12 +31,16 @@
 // section (masked probabilities and their score gradients are 0); the same
 // mask, statistics and scale as the forward.
 //
-// The main kernel is persistent: one CTA per SM walks a fixed list of units
-// (key tile, KV head, batch row), heavy first and in alternating directions
-// block by block.  Per-tile barrier phases run on across units; the next
-// unit's K/V load waits for the current unit's last MMA (kv_empty) and its
-// first dV/dK products for the epilogue's TMEM reads (dkv_empty), so a unit's
-// drain and epilogue overlap the next unit's first tiles.
+// The main kernel is persistent: one CTA per SM walks a fixed list of units,
+// heavy first and in alternating directions block by block.  The list is
+// key-tile-major inside groups of (batch row, KV head) pairs, sized by the
+// launcher so that a group's dQ accumulators and Q/dO tiles stay in L2 once
+// all of them would not.  Per-tile barrier phases run on across units; the
+// next unit's K/V load waits for the current unit's last MMA (kv_empty) and
+// its first dV/dK products for the epilogue's TMEM reads (dkv_empty), so a
+// unit's drain and epilogue overlap the next unit's first tiles.  The
+// producer prefetches each tile's Q and dO into L2 while it waits for the
+// tile's stage.
 //
 // Warp roles (448 threads): warps 0-7 compute (one key row = one TMEM lane per
 // thread; warps w and w+4 share the lanes of group w and split the 128 query
