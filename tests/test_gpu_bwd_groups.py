@@ -43,3 +43,38 @@ def test_grouped_backward_rows(B, Hq, Hkv, S):
         check_grad(to_np(dq[sl]), rq, f"dQ[{b}]")
         check_grad(to_np(dk[sl]), rk, f"dK[{b}]")
         check_grad(to_np(dv[sl]), rv, f"dV[{b}]")
+
+
+def test_grouped_backward_packed_sequences():
+    # 41 packed sequences x 16 KV heads = 656 pairs sized by the longest (512)
+    # sequence: five groups of 128 pairs and one of 16.  Lengths are ragged,
+    # so many units of a group are partial or empty.
+    nseq, H, d = 41, 16, 128
+    g = torch.Generator().manual_seed(141)
+    lens = torch.randint(64, 513, (nseq,), generator=g)
+    lens[0] = 512
+    cu = torch.zeros(nseq + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0)
+    total = int(cu[-1])
+    t = workloads.random_qkv(1, H, H, total, total, d, seed=142, with_dout=True)
+    q, k, v, do = (t[n][0] for n in ("q", "k", "v", "dout"))  # [H, total, d]
+    scale = 1.0 / math.sqrt(d)
+    cud = cu.to(DEV)
+    L = int(lens.max())
+    o, lse = fa.fa_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cud, cud, L, L, True, scale)
+    dq, dk, dv = fa.fa_bwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), o, do.to(DEV), lse, cud, cud,
+                                  L, L, True, scale)
+    torch.cuda.synchronize()
+    st, word = fa.fa_device_status()
+    assert st == 0, hex(word)
+    for s in (0, nseq // 2, nseq - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        sub = {n: x[:, a:b][None].contiguous() for n, x in (("q", q), ("k", k), ("v", v),
+                                                           ("dout", do))}
+        ro, rl = orc.fwd(sub["q"], sub["k"], sub["v"], True, scale)
+        check_o(to_np(o[:, a:b])[None], ro)
+        check_lse(to_np(lse[:, a:b])[None], rl)
+        rq, rk, rv = orc.bwd(sub["q"], sub["k"], sub["v"], sub["dout"], True, scale)
+        check_grad(to_np(dq[:, a:b])[None], rq, f"dQ[seq {s}]")
+        check_grad(to_np(dk[:, a:b])[None], rk, f"dK[seq {s}]")
+        check_grad(to_np(dv[:, a:b])[None], rv, f"dV[seq {s}]")
