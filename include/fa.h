@@ -264,6 +264,9 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
  *     array are rejected with FA_ERR_WORKSPACE before any device work.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is tied to the device's CUDA context: after cudaDeviceReset
+ *     (or with another context current) the next call looks it up again, so
+ *     that call, too, should come before any capture.
  *   - All calls on a device share the array: calls that can overlap on the GPU
  *     (different streams without ordering between them) race and corrupt each
  *     other's results.  Calls ordered on one stream are safe; nothing in the

@@ -4,7 +4,9 @@ io_aware_exact_tcgen05_gb300/libfa.so.  No cmake, no torch extension."""
 from __future__ import annotations
 
 import concurrent.futures as cf
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -30,15 +32,39 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _deps_mtime():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(ROOT, "include", "fa.h"))
+STAMP = LIB + ".sha256"
+
+
+def _fingerprint(extra_flags=()) -> str:
+    """Hash of every input of the build: the sources and headers (names and
+    contents), this script, the compiler flags and the host machine type.  A
+    library is reused only when its recorded fingerprint matches, so a copied
+    tree whose libfa.so is newer than its sources, or one built on another
+    machine type, is rebuilt all the same."""
+    h = hashlib.sha256()
+    files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                   if f.endswith((".cu", ".cuh", ".h")))
+    files += [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))]
     files.append(os.path.abspath(__file__))
-    return max(os.path.getmtime(f) for f in files)
+    for f in files:
+        h.update(os.path.basename(f).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join([*NVCC_FLAGS, *extra_flags]).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
+def _up_to_date(fp: str) -> bool:
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
+        return False
+    with open(STAMP) as fh:
+        return fh.read().strip() == fp
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
+    fp = _fingerprint(extra_flags)
+    if not force and _up_to_date(fp):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
@@ -65,6 +91,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP + f".tmp{os.getpid()}", "w") as fh:
+        fh.write(fp + "\n")
+    os.replace(STAMP + f".tmp{os.getpid()}", STAMP)
     return LIB
 
 

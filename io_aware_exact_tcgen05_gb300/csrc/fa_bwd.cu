@@ -712,25 +712,24 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          cudaStream_t stream) {
   constexpr size_t smem = sizeof(BwdSmem<D>);
   static_assert(smem <= 232448, "backward shared memory exceeds the per-CTA limit");
-  static bool configured[2] = {false, false};
   const bool drop = p.drop.on != 0;
-  if (!configured[drop]) {
-    cudaError_t e = cudaFuncSetAttribute(drop ? fa_bwd_main<D, true> : fa_bwd_main<D, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured[drop] = true;
-  }
+  // per-device kernel attribute: set on every call for the current device
+  cudaError_t e = cudaFuncSetAttribute(drop ? fa_bwd_main<D, true> : fa_bwd_main<D, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
   const long long pre_threads = rows * (D / 8);
   fa_bwd_pre<D><<<static_cast<unsigned int>((pre_threads + 255) / 256), 256, 0, stream>>>(p, rows);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (shared memory allows one) over the unit list
-  int dev = 0, n_sm = 0;
+  int dev = 0, n_sm = 0, l2_bytes = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev);
   if (e != cudaSuccess) return e;
+  const long long l2 = std::max(1LL << 20, static_cast<long long>(l2_bytes));
   const long long units = static_cast<long long>(p.n_kt) * p.grid_b * p.Hkv;
   const unsigned int grid = static_cast<unsigned int>(std::min<long long>(units, n_sm));
   // Pairs per group.  A pair's dQ accumulators and Q/dO tiles take 8 bytes
@@ -747,8 +746,8 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     const long long rows = p.cu_q ? static_cast<long long>(p.n_kt) * kTileN : p.Sq;
     const long long per_pair = std::max(1LL, 8LL * rows * D * p.group);
     long long g = pairs;
-    if (per_pair > (256LL << 20) / std::max(1LL, pairs)) {  // pairs * per_pair, without overflow
-      const long long fit = std::max(1LL, (64LL << 20) / per_pair);
+    if (per_pair > (2 * l2) / std::max(1LL, pairs)) {  // pairs * per_pair, without overflow
+      const long long fit = std::max(1LL, (l2 / 2) / per_pair);
       const long long waves = (3LL * n_sm + p.n_kt - 1) / std::max(1, p.n_kt);
       const long long t = std::max(fit, waves);
       if (t >= p.Hkv) {

@@ -267,9 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int o = LPK; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float m_new = fmaxf(m, mx);
       // the first finite max is always taken (also when c = 0); before it
-      // nothing is accumulated, so its rescale factor is 0
+      // nothing is accumulated, so its rescale factor is 0.  m_new - m is
+      // formed only once m is finite, so -inf - (-inf) is never evaluated.
       const bool first = (m == neg_inf()) && (m_new != neg_inf());
-      const bool grow = first || (m_new - m) * c > 0.f;  // NaN (both -inf) -> false
+      const bool grow = first || (m != neg_inf() && (m_new - m) * c > 0.f);
       if (__any_sync(0xffffffffu, grow)) {
         const float alpha = first ? 0.f : (grow ? ex2_approx((m - m_new) * c) : 1.f);
         l *= alpha;
@@ -394,14 +395,11 @@ __global__ void __launch_bounds__(D) fa_decode_merge(const DecodeParams p) {
 template <int D, int HG>
 cudaError_t launch_partial(const DecodeParams& p, int heads_per_cta, cudaStream_t stream) {
   const size_t smem = sizeof(DecodeSmem<D>) + 128;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_decode_partial<D, HG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // per-device kernel attribute: set on every call for the current device
+  cudaError_t e = cudaFuncSetAttribute(fa_decode_partial<D, HG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   const int n_hsub = (p.group + heads_per_cta - 1) / heads_per_cta;
   dim3 grid(p.n_split, p.Hkv * n_hsub, p.B);
   hook_before(stream);

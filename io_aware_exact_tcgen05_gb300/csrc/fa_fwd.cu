@@ -518,9 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // A row's first visible key always sets its max (also when c = 0,
           // where (m_new - m) * c would be inf * 0); nothing is accumulated
           // yet, so the rescale factor is 0.  Later the max moves only when it
-          // grows by more than the threshold.
+          // grows by more than the threshold.  The difference m_new - m is
+          // formed only once m is finite: a row that still sees no key keeps
+          // m = -inf and never evaluates -inf - (-inf).
           const bool first = (m == neg_inf()) && (m_new != neg_inf());
-          grow = first || (m_new - m) * c > p.rescale_log2;
+          grow = first || (m != neg_inf() && (m_new - m) * c > p.rescale_log2);
           alpha = first ? 0.f : (grow ? ex2_approx((m - m_new) * c) : 1.f);
           if (grow) {
             l *= alpha;
@@ -621,18 +623,17 @@ template <int D, int MODE>
 cudaError_t launch_fwd_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const FwdParams& p, cudaStream_t stream) {
   constexpr size_t smem = fwd_smem_bytes<D>();
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // The shared-memory limit is a per-device attribute of the kernel: it is
+  // set on every call, for whichever device is current (no process-wide
+  // state, so several devices, threads and device resets need no care).
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (shared memory allows one), each walking the
   // heavy-first unit list with stride gridDim.x
   int dev = 0, n_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   // Packed ragged batches keep one unit per CTA: their unit costs vary with

@@ -341,8 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < kTileN; jj += 2)
             mx = max3f(mx, __uint_as_float(sr[jj]), __uint_as_float(sr[jj + 1]));
           const float m_new = fmaxf(m, mx);
+          // the difference is formed only once m is finite (no -inf - (-inf))
           const bool first = (m == neg_inf()) && (m_new != neg_inf());
-          grow = first || (m_new - m) * c > p.rescale_log2;
+          grow = first || (m != neg_inf() && (m_new - m) * c > p.rescale_log2);
           alpha = first ? 0.f : (grow ? ex2_approx((m - m_new) * c) : 1.f);
           if (grow) {
             l *= alpha;
@@ -431,14 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
                            const Fp8FwdParams& p, cudaStream_t stream) {
   constexpr size_t smem = sizeof(Fp8Smem) + 1024;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_fp8_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // per-device kernel attribute: set on every call for the current device
+  const cudaError_t e = cudaFuncSetAttribute(fa_fwd_fp8_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   const unsigned int grid = static_cast<unsigned int>(p.n_rbu) * p.units_per_rbu;
   hook_before(stream);
   fa_fwd_fp8_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tvt, p);

@@ -16,7 +16,9 @@ central differences, and the gradient invariants of the chain-rule section.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 
@@ -29,14 +31,34 @@ _lock = threading.Lock()
 _lib = None
 
 
+_CMD = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11"]
+_STAMP = _LIB + ".sha256"
+
+
+def _fingerprint() -> str:
+    """Hash of the source, the compiler command and the machine type: the
+    library is reused only when the recorded hash matches."""
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as fh:
+        h.update(fh.read())
+    h.update(" ".join(_CMD).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
     """Compile fa_oracle.c into liboracle.so (gcc, OpenMP, no -march flags)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
-        return _LIB
+    fp = _fingerprint()
+    if not force and os.path.exists(_LIB) and os.path.exists(_STAMP):
+        with open(_STAMP) as fh:
+            if fh.read().strip() == fp:
+                return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    subprocess.run([*_CMD, _SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _LIB)
+    with open(_STAMP + f".tmp{os.getpid()}", "w") as fh:
+        fh.write(fp + "\n")
+    os.replace(_STAMP + f".tmp{os.getpid()}", _STAMP)
     return _LIB
 
 

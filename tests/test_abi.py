@@ -56,10 +56,15 @@ def test_fwd_validation_before_any_device_call(lib):
     assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
     assert _fwd(lib, q=0) == fa.FA_ERR_INVALID_ARG
     assert _fwd(lib, o=18) == fa.FA_ERR_INVALID_ARG  # misaligned
+    assert lib.fa_last_error_detail() == b"o is not 16-byte aligned"
     assert _fwd(lib, lse=8) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_last_error_detail() == b"lse is not 16-byte aligned"
     assert _fwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert b"scale" in lib.fa_last_error_detail()
     assert _fwd(lib, scale=-0.5) == fa.FA_ERR_INVALID_ARG
-    assert b"16-byte" in lib.fa_last_error_detail() or True
+    assert b"must be finite and >= 0" in lib.fa_last_error_detail()
+    assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert b"head dimension 96" in lib.fa_last_error_detail()
 
 
 def test_status_strings(lib):
