@@ -4,26 +4,35 @@
 //   2. fa_bwd_main:  work units of (128-key tile, KV head, batch row).  K and
 //                    V stay in shared memory; a unit walks every query head of
 //                    the group and every 128-row query tile that can see its
-//                    keys.  Per query tile (all five contractions on tcgen05):
+//                    keys.  Per query tile i (all five contractions on tcgen05):
 //        S^T  = K Q^T            (keys x queries, fp32 in TMEM)
 //        dP^T = V dO^T           (keys x queries, fp32 in TMEM)
 //        P^T  = exp(scale*S^T - LSE) on visible entries, 0 elsewhere
 //               -> bf16 back into the S^T columns           [compute warps]
 //        dV  += P^T dO           (A = P^T from TMEM)
-//        dS^T = P^T * (dP^T - D) -> bf16 into the dP^T columns and into
-//               shared memory                               [compute warps]
-//        dK  += dS^T Q           (A = dS^T from TMEM)
-//        dQ   = dS K             (A = dS from shared memory, written into the
-//                                 dP^T columns, which are free by then)
-//        dQacc += dQ             TMEM -> shared (this tile's Q and dO stage,
-//                                free once dK and dV have read it) -> TMA
-//                                reduce-add into the fp32 accumulator
-//                                                            [drain warps]
-//      The stage is refilled (two tiles later) only after the drain's reduces
-//      have read it, so the drain never delays the compute warps.
+//        dS^T = P^T * (dP^T - D) -> bf16 into shared memory [compute warps]
+//        dQ   = dS K             (A = dS from shared memory, into the dP^T
+//                                 columns, which the compute warps have read)
+//        dK  += dS^T Q           (A = the same shared dS^T rows, K-major)
+//        dQacc += dQ             TMEM -> registers -> 32 KB of staging in
+//                                shared memory -> TMA reduce-add into the fp32
+//                                accumulator                 [drain warps]
 //      At the end dK (times scale) and dV leave TMEM as bf16.  With grouped
 //      heads dK/dV already hold the sum over the group's query heads.
 //   3. fa_bwd_convert: dQ = bf16(scale * dQacc)
+//
+// Issue order per tile: dP^T(i), dV(i), S^T(i+1), dQ(i), dK(i).
+//   * S^T(i+1) follows dV(i), which has read P^T(i) from the S^T columns, so
+//     P(i+1) is computed while dQ(i), dK(i) and dP^T(i+1) run.
+//   * dQ(i) goes before dK(i): dK reads dS^T from shared memory, not from
+//     TMEM, so dQ may overwrite the dP^T columns as soon as every compute
+//     warp has loaded dP^T(i).  The drain of dQ(i) then overlaps dK(i).
+//   * dP^T(i+1) waits for the drain to have read dQ(i) out of TMEM; this
+//     loop (dQ -> drain -> dP^T -> dS -> dQ) sets the pace.
+// Q is double-buffered (S^T(i+1) is issued before dK(i) has read Q(i)); dO
+// has one buffer, refilled as soon as dV(i) has read it, which leaves dK(i),
+// dQ(i) and S^T(i+1) to cover the load.  The dQ staging is separate from
+// both, so refilling a Q/dO buffer never waits for a reduce-add.
 //
 // Method: FlashAttention_01 page, "why the backward can recompute" (rebuild P
 // from the saved per-row logsumexp; dV and dP first, then dS from the softmax
@@ -45,7 +54,8 @@
 // Warp roles (448 threads): warps 0-7 compute (one key row = one TMEM lane per
 // thread; warps w and w+4 share the lanes of group w and split the 128 query
 // columns, so P and dS need no cross-warp exchange), warps 8-11 drain dQ (one
-// query row per thread), warp 12 TMA producer, warp 13 MMA issuer and TMEM owner.
+// query row per thread, 8 KB of staging each), warp 12 TMA producer, warp 13
+// MMA issuer and TMEM owner.
 #include <algorithm>
 
 #include <cuda_runtime.h>
@@ -69,7 +79,7 @@ constexpr int kQStages = 2;
 
 enum : unsigned int {
   kSiteKV = 1, kSiteQFull, kSiteQEmpty, kSiteS, kSiteP, kSiteDP, kSiteDS, kSiteDQFull,
-  kSiteDQEmpty, kSiteDKV, kSiteDrain, kSiteAlign, kSiteStat
+  kSiteDQEmpty, kSiteDKV, kSiteDrain, kSiteAlign, kSiteStat, kSiteDOFull, kSiteDOEmpty
 };
 
 template <int D>
@@ -79,13 +89,15 @@ struct BwdSmem {
   __nv_bfloat16 k[NB][kBox];
   __nv_bfloat16 v[NB][kBox];
   __nv_bfloat16 q[kQStages][NB][kBox];
-  __nv_bfloat16 dout[kQStages][NB][kBox];
+  __nv_bfloat16 dout[NB][kBox];     // one buffer: dO(i+1) loads while dK/dQ(i) and S^T(i+1) run
   __nv_bfloat16 ds[2][kBox];        // dS^T rows = keys, two 64-query blocks, 128B swizzle
+  float dq_stage[4][2][32 * 32];    // per drain warp: two 32x32 fp32 boxes, 128B swizzle
   float nlse2[2][kTileM];           // -LSE * log2(e), -inf for rows without keys
   float ndelta[2][kTileM];          // -D_i; both double-buffered by tile parity
   uint64_t stat_ready[2];
   uint64_t kv_full;
   uint64_t q_full[kQStages], q_empty[kQStages];
+  uint64_t do_full, do_empty;
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_empty, dkv_full, drain;
   uint64_t kv_empty, dkv_empty;  // hand-over between consecutive units
   uint32_t tmem_base;
@@ -230,8 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.kv_full, 1);
     for (int i = 0; i < kQStages; ++i) {
       mbar_init(&s.q_full[i], 1);
-      mbar_init(&s.q_empty[i], 1 + 4);  // MMA commit + the 4 dQ drain warps
+      mbar_init(&s.q_empty[i], 1);  // MMA commit after the tile's last product
     }
+    mbar_init(&s.do_full, 1);
+    mbar_init(&s.do_empty, 1);  // MMA commit after dV
     mbar_init(&s.s_full, 1);
     mbar_init(&s.p_full, 8);  // one arrival per compute warp
     mbar_init(&s.dp_full, 1);
@@ -255,11 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
-  // P^T (bf16) of query half hf sits in S^T columns [64 hf, 64 hf + 32) and
-  // dS^T in dP^T columns [64 hf, 64 hf + 32): inside the columns that half's
-  // own warps read, so neither half overwrites scores the other still needs.
+  // P^T (bf16) of query half hf sits in S^T columns [64 hf, 64 hf + 32):
+  // inside the columns that half's own warps read, so neither half
+  // overwrites scores the other still needs.
   const uint32_t t_S = tmem;              // S^T, then P^T
-  const uint32_t t_dP = tmem + kTileN;    // dP^T, then dS^T, then dQ
+  const uint32_t t_dP = tmem + kTileN;    // dP^T, then dQ
   const uint32_t t_dV = tmem + 2 * kTileN;
   const uint32_t t_dK = tmem + 2 * kTileN + D;
   volatile int* abort_flag = &s.abort_flag;
@@ -275,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tv);
       tma_prefetch_desc(&tdo);
       int ig = 0, uk = 0;  // iterations and K/V loads issued so far
-      int issued = 0;
+      int issued = 0, do_issued = 0;
       bool ok = true;
       for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
         const int U = unit_index(k);
@@ -307,18 +321,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&s.q_full[st], 2 * NB * kBoxBytes);
-          for (int cb = 0; cb < NB; ++cb) {
+          mbar_arrive_expect_tx(&s.q_full[st], NB * kBoxBytes);
+          for (int cb = 0; cb < NB; ++cb)
             tma_load_3d(s.q[st][cb], &tq, &s.q_full[st], cb * 64, un.qb + q0, zq);
-            tma_load_3d(s.dout[st][cb], &tdo, &s.q_full[st], cb * 64, un.qb + q0, zq);
-          }
           issued = ig + 1;
+          // dO has one buffer, free once dV of the previous tile has read it
+          if (ig > 0 && !mbar_wait(&s.do_empty, (ig - 1) & 1, abort_flag, kSiteDOEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.do_full, NB * kBoxBytes);
+          for (int cb = 0; cb < NB; ++cb)
+            tma_load_3d(s.dout[cb], &tdo, &s.do_full, cb * 64, un.qb + q0, zq);
+          do_issued = ig + 1;
         }
       }
       if (*abort_flag) {
         if (uk > 0) mbar_drain(&s.kv_full, (uk - 1) & 1, kSiteDrain);
         for (int i = max(0, issued - kQStages); i < issued; ++i)
           mbar_drain(&s.q_full[i % kQStages], (i / kQStages) & 1, kSiteDrain);
+        if (do_issued > 0) mbar_drain(&s.do_full, (do_issued - 1) & 1, kSiteDrain);
       }
     }
   } else if (warp == kWarpMma) {
@@ -339,10 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t v_kmaj = smem_desc_sw128(smem_u32(s.v[0]), 16, 1024);
       const uint64_t k_mn = smem_desc_sw128(smem_u32(s.k[0]), kLbo, 1024);
       const uint64_t q_kmaj0 = smem_desc_sw128(smem_u32(s.q[0][0]), 16, 1024);
-      const uint64_t o_kmaj0 = smem_desc_sw128(smem_u32(s.dout[0][0]), 16, 1024);
+      const uint64_t o_kmaj0 = smem_desc_sw128(smem_u32(s.dout[0]), 16, 1024);
       const uint64_t q_mn0 = smem_desc_sw128(smem_u32(s.q[0][0]), kLbo, 1024);
-      const uint64_t o_mn0 = smem_desc_sw128(smem_u32(s.dout[0][0]), kLbo, 1024);
+      const uint64_t o_mn0 = smem_desc_sw128(smem_u32(s.dout[0]), kLbo, 1024);
       const uint64_t ds_mn = smem_desc_sw128(smem_u32(s.ds[0]), kBoxBytes, 1024);
+      const uint64_t ds_kmaj = smem_desc_sw128(smem_u32(s.ds[0]), 16, 1024);
       int ig = 0, uk = 0;
       bool ok = true;
       for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
@@ -357,19 +380,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Q and dO arrive by TMA (the mbarrier wait orders them before the
           // MMAs); the S^T columns this overwrites were last touched by other
           // threads before p_full of the previous tile, whose fence covers them.
-          if (!mbar_wait_warp(&s.q_full[st], (ig / kQStages) & 1, abort_flag, kSiteQFull)) {
+          if (it == 0) {
+            if (!mbar_wait_warp(&s.q_full[st], (ig / kQStages) & 1, abort_flag, kSiteQFull)) {
+              ok = false;
+              break;
+            }
+            // S^T = K Q^T  (A = K rows, B = Q rows, both K-major over d)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+              mma_ss_warp(t_S, desc_add(k_kmaj, off), desc_add(q_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_warp(&s.s_full);
+          }
+          // dP^T = V dO^T; its columns held dQ of the previous tile
+          if (ig > 0 && !mbar_wait_warp(&s.dq_empty, (ig - 1) & 1, abort_flag, kSiteDQEmpty)) {
             ok = false;
             break;
           }
-          // S^T = K Q^T  (A = K rows, B = Q rows, both K-major over d)
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss_warp(t_S, desc_add(k_kmaj, off), desc_add(q_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
-          }
-          mma_commit_warp(&s.s_full);
-          // dP^T = V dO^T; its columns held dQ of the previous tile
-          if (ig > 0 && !mbar_wait_warp(&s.dq_empty, (ig - 1) & 1, abort_flag, kSiteDQEmpty)) {
+          if (!mbar_wait_warp(&s.do_full, ig & 1, abort_flag, kSiteDOFull)) {
             ok = false;
             break;
           }
@@ -377,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss_warp(t_dP, desc_add(v_kmaj, off), desc_add(o_kmaj0, so + off), id_kq, kk > 0 ? 1u : 0u);
+            mma_ss_warp(t_dP, desc_add(v_kmaj, off), desc_add(o_kmaj0, off), id_kq, kk > 0 ? 1u : 0u);
           }
           mma_commit_warp(&s.dp_full);
           // dV += P^T dO  (A = P^T in TMEM; B = dO rows, MN-major over d)
@@ -388,29 +417,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          mma_ts_warp(t_dV, t_S, desc_add(o_mn0, so), id_acc, it > 0 ? 1u : 0u);
+          mma_ts_warp(t_dV, t_S, o_mn0, id_acc, it > 0 ? 1u : 0u);
 #pragma unroll
           for (int kk = 1; kk < kTileM / 16; ++kk)
-            mma_ts_warp(t_dV, t_S + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(o_mn0, so + kk * 2048),
+            mma_ts_warp(t_dV, t_S + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(o_mn0, kk * 2048),
                    id_acc, 1u);
-          // dK += dS^T Q  (A = dS^T in TMEM; B = Q rows, MN-major over d)
+          mma_commit_warp(&s.do_empty);  // dO has been read: the next tile's may load
+          // next tile's S^T now: the pipe runs dV before it, so P^T has been read
+          if (it + 1 < un.n_it) {
+            const int st1 = (ig + 1) % kQStages;
+            const uint32_t so1 = static_cast<uint32_t>(st1) * kStage;
+            if (!mbar_wait_warp(&s.q_full[st1], ((ig + 1) / kQStages) & 1, abort_flag, kSiteQFull)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+              mma_ss_warp(t_S, desc_add(k_kmaj, off), desc_add(q_kmaj0, so1 + off), id_kq, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_warp(&s.s_full);
+          }
+          // dS is complete in shared memory and dP^T has been read into registers
           if (!mbar_wait_warp(&s.ds_full, ig & 1, abort_flag, kSiteDS)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          mma_ts_warp(t_dK, t_dP, desc_add(q_mn0, so), id_acc, it > 0 ? 1u : 0u);
-#pragma unroll
-          for (int kk = 1; kk < kTileM / 16; ++kk)
-            mma_ts_warp(t_dK, t_dP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(q_mn0, so + kk * 2048),
-                   id_acc, 1u);
           // dQ = dS K  (A = dS: shared rows = keys, queries contiguous -> MN-major;
-          //             B = K rows, d contiguous -> MN-major), into the dP^T columns
+          //             B = K rows, d contiguous -> MN-major), into the dP^T columns.
+          // Issued before dK so that the drain of dQ overlaps dK.
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
             mma_ss_warp(t_dP, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), id_dq,
                    kk > 0 ? 1u : 0u);
           mma_commit_warp(&s.dq_full);
+          // dK += dS^T Q  (A = dS^T: the same shared rows = keys, queries contiguous
+          //               -> K-major; B = Q rows, MN-major over d)
+#pragma unroll
+          for (int kk = 0; kk < kTileM / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_ss_warp(t_dK, desc_add(ds_kmaj, off), desc_add(q_mn0, so + kk * 2048), id_acc,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+          }
           mma_commit_warp(&s.q_empty[st]);
         }
         if (!ok) break;
@@ -571,15 +620,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             f2_unpack(f2_mul(bf16x2_to_f2(pk[cc * 16 + e]), dp2), d0, d1);
             dw[e] = pack_bf16x2(d0, d1);
           }
-          tmem_st16(t_dP + lane_off + hf * 64 + cc * 16, dw);
-          // shared copy: 32 queries = four 16-byte chunks of query block hf
+          // dS^T to shared memory only: 32 queries = four 16-byte chunks of query block hf
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             const uint32_t chunk = static_cast<uint32_t>((cc * 4 + ch) ^ (row & 7));
             st_shared_v4(blk + chunk * 16, dw[4 * ch], dw[4 * ch + 1], dw[4 * ch + 2], dw[4 * ch + 3]);
           }
         }
-        tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -638,14 +685,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     // --------------------------------------------- dQ drain (warps 8-11) --
-    // Each warp moves its 32 query rows of dQ from TMEM into a 128*d-byte slice
-    // of this tile's Q/dO stage (32-column boxes, 128-byte swizzle; warps 0-1
-    // of the group use the Q buffer, 2-3 the dO buffer) and hands them to TMA
-    // reduce-add.  The stage is released to the producer once TMA has read it.
+    // Each warp moves its 32 query rows of dQ from TMEM to global memory with
+    // TMA reduce-adds through its own 8 KB of staging (two 32x32 fp32 boxes,
+    // 128-byte swizzle).  With d = 128 the row is staged in two halves: the
+    // first 64 columns go to shared memory and the last 64 are held in
+    // registers, so TMEM is released after one pass; the second half waits
+    // only for the first half's reduces to have read the staging.
     const int wq = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    constexpr int kSlice = 32 * D * 4;  // bytes of one warp's rows
-    int ig = 0;  // iterations across the CTA's units (barrier phases, stages)
+    unsigned char* region = reinterpret_cast<unsigned char*>(&s.dq_stage[wq][0][0]);
+    const uint32_t region_u32 = smem_u32(region);
+    auto stage_64 = [&](const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
+      const uint32_t b0 = region_u32 + lane * 128, b1 = region_u32 + 4096 + lane * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        st_shared_v4(b0 + ((ch ^ (lane & 7)) * 16), r0[4 * ch], r0[4 * ch + 1], r0[4 * ch + 2], r0[4 * ch + 3]);
+        st_shared_v4(b1 + ((ch ^ (lane & 7)) * 16), r1[4 * ch], r1[4 * ch + 1], r1[4 * ch + 2], r1[4 * ch + 3]);
+      }
+    };
+    int ig = 0;  // iterations across the CTA's units (barrier phases)
     bool ok = true;
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
       const int U = unit_index(k);
@@ -656,26 +714,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = it / un.n_qt;
         const int q0 = (un.qt_lo + it % un.n_qt) * kTileM;
         const int h = un.hk * p.group + g;
-        const int st = ig % kQStages;
-        unsigned char* region = reinterpret_cast<unsigned char*>(
-                                    wq < 2 ? &s.q[st][0][0] : &s.dout[st][0][0]) +
-                                (wq & 1) * kSlice;
-        const uint32_t region_u32 = smem_u32(region);
+        const int row = un.qb + q0 + wq * 32;
+        const int zz = un.bz * p.Hq + h;
         if (!mbar_wait_warp(&s.dq_full, ig & 1, abort_flag, kSiteDQFull)) {
           ok = false;
           break;
         }
         tc_fence_after();
-#pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx) {
-          uint32_t r[32];
-          tmem_ld32(t_dP + lane_off + bx * 32, r);
+        uint32_t r0[32], r1[32];
+        tmem_ld32(t_dP + lane_off, r0);
+        tmem_ld32(t_dP + lane_off + 32, r1);
+        tmem_wait_ld();
+        // the previous tile's reduces must have read the staging (waiting at
+        // the end of that tile instead measured slower)
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        stage_64(r0, r1);
+        if constexpr (D == 128) {
+          tmem_ld32(t_dP + lane_off + 64, r0);
+          tmem_ld32(t_dP + lane_off + 96, r1);
           tmem_wait_ld();
-          const uint32_t base = region_u32 + bx * 4096 + lane * 128;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            st_shared_v4(base + ((ch ^ (lane & 7)) * 16), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2],
-                         r[4 * ch + 3]);
         }
         // dQ is out of TMEM: dP^T of the next tile may reuse the columns
         tc_fence_before();
@@ -684,13 +742,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-#pragma unroll
-          for (int bx = 0; bx < D / 32; ++bx)
-            tma_reduce_add_3d(&tdq, region + bx * 4096, bx * 32, un.qb + q0 + wq * 32,
-                              un.bz * p.Hq + h);
+          tma_reduce_add_3d(&tdq, region, 0, row, zz);
+          tma_reduce_add_3d(&tdq, region + 4096, 32, row, zz);
           bulk_commit_group();
-          bulk_wait_read0();
-          mbar_arrive(&s.q_empty[st]);
+        }
+        if constexpr (D == 128) {
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+          stage_64(r0, r1);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tdq, region, 64, row, zz);
+            tma_reduce_add_3d(&tdq, region + 4096, 96, row, zz);
+            bulk_commit_group();
+          }
         }
         __syncwarp();
       }
