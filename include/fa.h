@@ -176,14 +176,16 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
  * can recompute", "interface and implementation constraints" and "training
  * configuration and misuse boundaries": recomputation needs the same mask,
  * statistics, scale and dropout mapping).
- *   O_i = sum_j P_ij * keep_ij / (1 - p) * v_j,  P the undropped softmax;
+ *   O_i = sum_j P_ij * keep_ij * r * v_j,  P the undropped softmax;
  *   LSE is the undropped one (what the backward needs to rebuild P).
  *   keep_ij <=> the 16-bit half (j mod 2) (0: low, 1: high) of word
  *   ((j mod 8) / 2) of Philox4x32-10 (Salmon et al., SC 2011) at counter
  *   (j / 8, i, b * Hq + h, offset) under key (seed & 0xffffffff, seed >> 32)
- *   is >= floor(dropout_p * 2^16); i is the query row and j the key index
- *   within batch row b.  The keep probability is thus 1 - floor(p * 2^16) / 2^16
- *   (p below 2^-16 keeps every weight, still scaled by 1 / (1 - p)).
+ *   is >= thr = floor(dropout_p * 2^16); i is the query row and j the key
+ *   index within batch row b.  The keep probability is thus 1 - thr / 2^16,
+ *   and kept weights are scaled by its reciprocal r = 2^16 / (2^16 - thr),
+ *   so E[keep_ij * r] = 1 exactly (p below 2^-16: thr = 0, nothing is dropped
+ *   and r = 1).
  * dropout_p must lie in [0, 1) (0 = no dropout); the backward must get the
  * forward's dropout_p, seed and offset.  Otherwise these are fa_fwd_masked /
  * fa_bwd_masked (key_mask_bits may be NULL).

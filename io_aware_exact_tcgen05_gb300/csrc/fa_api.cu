@@ -222,19 +222,22 @@ fa_status check_key_bits(const uint32_t* bits) {
 }
 
 // Dropout arguments from the caller's probability, seed and offset: keep a
-// weight iff its 16-bit Philox draw is >= floor(p * 2^16) (computed in
-// double, the same integer threshold the reference computation uses).
+// weight iff its 16-bit Philox draw is >= thr = floor(p * 2^16) (computed in
+// double, the same integer threshold the reference computation uses); kept
+// weights are scaled by 2^16 / (2^16 - thr), the reciprocal of the keep
+// probability, so the dropped output is unbiased.
 fa_status make_dropout(float p_drop, unsigned long long seed, unsigned int offset,
                        fa::DropoutArgs* out) {
   if (!(p_drop >= 0.f && p_drop < 1.f))
     return fail(FA_ERR_INVALID_ARG, "dropout_p (%g) must lie in [0, 1)", (double)p_drop);
   fa::DropoutArgs dr{};
-  dr.thr_hi = static_cast<uint32_t>(std::floor(static_cast<double>(p_drop) * 65536.0)) << 16;
+  const uint32_t thr = static_cast<uint32_t>(std::floor(static_cast<double>(p_drop) * 65536.0));
+  dr.thr_hi = thr << 16;
   dr.on = p_drop > 0.f ? 1u : 0u;
   dr.seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
   dr.seed_hi = static_cast<uint32_t>(seed >> 32);
   dr.offset = offset;
-  dr.scale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop)));
+  dr.scale = static_cast<float>(65536.0 / (65536.0 - static_cast<double>(thr)));
   *out = dr;
   return FA_OK;
 }

@@ -37,7 +37,7 @@ struct DropoutArgs {
   uint32_t seed_lo;
   uint32_t seed_hi;
   uint32_t offset;
-  float scale;       // 1 / (1 - p)
+  float scale;       // 2^16 / (2^16 - floor(p * 2^16)): 1 / the keep probability
   uint32_t on;       // p > 0
 };
 

@@ -40,11 +40,13 @@
  * Dropout on the attention weights (FlashAttention_01 page, "why the
  * backward can recompute" and "interface and implementation constraints":
  * the random mask is part of the forward/backward contract and must be
- * reproduced element by element).  With probability p_drop, weight (i, j)
- * is dropped and the kept ones are scaled by 1 / (1 - p_drop):
- *   O_i   = u_i / l_i,  u_i = sum_vis exp(s_ij - m) keep_ij / (1 - p) v_j
+ * reproduced element by element).  Weight (i, j) is dropped with
+ * probability q = floor(p_drop * 2^16) / 2^16 (the draws are 16-bit) and the
+ * kept ones are scaled by r = 1 / (1 - q), so each weight keeps its
+ * expectation (inverted dropout):
+ *   O_i   = u_i / l_i,  u_i = sum_vis exp(s_ij - m) keep_ij r v_j
  *   (m, l and LSE are those of the undropped weights)
- *   dP_ij = keep_ij / (1 - p) <dO_i, v_j>,  dV_j = sum_i p_ij keep_ij / (1 - p) dO_i
+ *   dP_ij = keep_ij r <dO_i, v_j>,  dV_j = sum_i p_ij keep_ij r dO_i
  * keep_ij comes from Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel
  * random numbers: as easy as 1, 2, 3", SC 2011) with counter
  * (j / 8, i, b * Hq + h, offset) and key (seed low word, seed high word):
@@ -115,7 +117,7 @@ void oracle_philox4x32_10(const uint32_t* ctr, uint32_t k0, uint32_t k1, uint32_
 typedef struct {
   int on;
   uint32_t thr;          /* floor(p * 2^16): keep iff the 16-bit draw is >= thr */
-  double keep_scale;     /* 1 / (1 - p) */
+  double keep_scale;     /* 2^16 / (2^16 - thr): 1 / the keep probability */
   uint32_t seed_lo, seed_hi, offset;
 } drop_t;
 
@@ -123,14 +125,14 @@ static drop_t make_drop(double p, unsigned long long seed, unsigned int offset) 
   drop_t d;
   d.on = p > 0.0;
   d.thr = d.on ? (uint32_t)floor(p * 65536.0) : 0u;
-  d.keep_scale = d.on ? 1.0 / (1.0 - p) : 1.0;
+  d.keep_scale = d.on ? 65536.0 / (65536.0 - (double)d.thr) : 1.0;
   d.seed_lo = (uint32_t)(seed & 0xffffffffull);
   d.seed_hi = (uint32_t)(seed >> 32);
   d.offset = offset;
   return d;
 }
 
-/* keep_ij / (1 - p) for query row i of query head bh (= b * Hq + h), key j */
+/* keep_ij / P(keep) for query row i of query head bh (= b * Hq + h), key j */
 static double drop_factor(const drop_t* d, long bh, long i, long j) {
   if (!d || !d->on) return 1.0;
   const uint32_t ctr[4] = {(uint32_t)(j / 8), (uint32_t)i, (uint32_t)bh, d->offset};

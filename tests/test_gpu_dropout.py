@@ -2,8 +2,9 @@
 FP64 oracle's Philox4x32-10 mapping: the keep decisions must agree exactly
 (they are integer comparisons of 16-bit draws on both sides), and O, LSE, dQ,
 dK, dV within the usual tolerances.  Probabilities are exact in float32, so
-both sides use the same integer threshold; 2^-17 has threshold 0 (every
-weight kept, and still scaled by 1 / (1 - p))."""
+both sides use the same integer threshold thr = floor(p * 2^16); kept weights
+are scaled by 2^16 / (2^16 - thr), and 2^-17 has threshold 0 (every weight
+kept, unscaled)."""
 import math
 
 import numpy as np
@@ -27,7 +28,7 @@ def _status_ok():
 @pytest.mark.parametrize("p", [0.25, 0.625, 2.0**-17])
 def test_keep_decisions_match_the_mapping_exactly(p):
     # scale 0: every visible key has weight 1/128; V row j is the unit vector
-    # e_(j - k0), so O[..., c] = keep(key k0 + c) / (1 - p) / 128 reads the
+    # e_(j - k0), so O[..., c] = keep(key k0 + c) * r / 128 reads the
     # mask off directly.  Keys 384..511 of batch row 1 exercise large key
     # indices; several heads and 200 rows vary the other counter words.
     B, H, Sq, Sk, d = 2, 3, 200, 512, 128
@@ -53,7 +54,8 @@ def test_keep_decisions_match_the_mapping_exactly(p):
                     want[b, h, i, c] = orc.dropout_keep(p, seed, off, b * H + h, i, k0 + c)
     assert np.array_equal(got, want), f"{int((got != want).sum())} decisions differ"
     kept = to_np(o)[got]
-    assert np.allclose(kept, 1.0 / (1.0 - p) / 128.0, rtol=1e-2)
+    thr = math.floor(p * 65536.0)
+    assert np.allclose(kept, 65536.0 / (65536.0 - thr) / 128.0, rtol=1e-2)
     assert np.allclose(to_np(lse), math.log(128.0), atol=1e-5)  # LSE of the undropped weights
 
 

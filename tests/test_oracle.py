@@ -366,14 +366,54 @@ def test_dropout_keep_rate_and_mapping():
     halves = [(int(x) >> s) & 0xFFFF for w in (w0, w1) for x in w for s in (0, 16)]
     assert [orc.dropout_keep(p, seed, off, 1, 3, j) for j in range(16)] == \
         [h >= int(p * 2**16) for h in halves]
-    # a probability below 2^-16 keeps every weight (its kept weights are still
-    # scaled by 1 / (1 - p))
+    # a probability below 2^-16 keeps every weight (threshold 0)
     assert all(orc.dropout_keep(1e-6, seed, off, 0, 3, j) for j in range(64))
     # p = 0 keeps everything; another seed or offset gives another mask
     assert all(orc.dropout_keep(0.0, seed, off, 0, 3, j) for j in range(64))
     a = [orc.dropout_keep(p, seed, off, 0, 3, j) for j in range(256)]
     assert a != [orc.dropout_keep(p, seed + 1, off, 0, 3, j) for j in range(256)]
     assert a != [orc.dropout_keep(p, seed, off + 1, 0, 3, j) for j in range(256)]
+
+
+def test_dropout_that_drops_nothing_is_the_plain_attention():
+    # p below 2^-16: every 16-bit draw is >= 0, so nothing is dropped, the
+    # keep probability is 1 and the result must be the undropped attention
+    B, Hq, Hkv, Sq, Sk, d = 1, 2, 1, 17, 29, 8
+    q = _rand((B, Hq, Sq, d), 90)
+    k = _rand((B, Hkv, Sk, d), 91)
+    v = _rand((B, Hkv, Sk, d), 92)
+    do = _rand((B, Hq, Sq, d), 93)
+    o0, l0 = orc.fwd(q, k, v, True, 0.3)
+    o1, l1 = orc.fwd(q, k, v, True, 0.3, dropout_p=2.0**-17, seed=5, offset=1)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    g0 = orc.bwd(q, k, v, do, True, 0.3)
+    g1 = orc.bwd(q, k, v, do, True, 0.3, dropout_p=2.0**-17, seed=5, offset=1)
+    for a, b in zip(g0, g1):
+        assert np.array_equal(a, b)
+
+
+def test_dropout_keeps_the_expectation():
+    # inverted dropout: averaged over many masks, the dropped output is the
+    # undropped one (the kept weights carry 1 / P(keep)); with the 16-bit
+    # threshold P(keep) = 1 - floor(p 2^16) / 2^16, which differs from 1 - p
+    # for p = 0.3, so the mean of keep * scale must be 1, not (1-q)/(1-p)
+    p, off = 0.3, 2
+    Sk, d = 64, 4
+    q = torch.zeros(1, 1, 1, d, dtype=torch.float64)
+    k = torch.zeros(1, 1, Sk, d, dtype=torch.float64)
+    v = torch.ones(1, 1, Sk, d, dtype=torch.float64)
+    # scale 0: uniform weights 1/Sk, so O = mean over keys of keep * scale
+    outs = [orc.fwd(q, k, v, False, 0.0, dropout_p=p, seed=s, offset=off)[0][0, 0, 0, 0]
+            for s in range(400)]
+    thr = math.floor(p * 65536)
+    r = 65536.0 / (65536.0 - thr)
+    kept = np.array(outs) / r * Sk  # kept keys per mask
+    assert np.allclose(kept, np.round(kept), atol=1e-9)  # O is (kept count) * r / Sk exactly
+    n = len(outs) * Sk
+    keep_rate = kept.sum() / n
+    sigma = math.sqrt((1 - thr / 65536) * (thr / 65536) / n)
+    assert abs(keep_rate - (1 - thr / 65536)) < 5 * sigma
+    assert abs(np.mean(outs) - 1.0) < 5 * sigma * r
 
 
 @pytest.mark.parametrize("causal", [False, True])
