@@ -75,7 +75,7 @@ constexpr int kThreads = 448;
 constexpr int kWarpProducer = 12;
 constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kQStages = 2;
+
 
 enum : unsigned int {
   kSiteKV = 1, kSiteQFull, kSiteQEmpty, kSiteS, kSiteP, kSiteDP, kSiteDS, kSiteDQFull,
@@ -84,6 +84,7 @@ enum : unsigned int {
 
 template <int D>
 struct BwdSmem {
+  static constexpr int kQStages = BwdTiles<D>::kQStages;
   static constexpr int NB = D / 64;
   static constexpr int kBox = kTileM * 64;
   __nv_bfloat16 k[NB][kBox];
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&s.kv_full, 1);
-    for (int i = 0; i < kQStages; ++i) {
+    for (int i = 0; i < Smem::kQStages; ++i) {
       mbar_init(&s.q_full[i], 1);
       mbar_init(&s.q_empty[i], 1);  // MMA commit after the tile's last product
     }
@@ -305,8 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++uk;
         for (int it = 0; it < un.n_it; ++it, ++ig) {
-          const int st = ig % kQStages;
-          const int use = ig / kQStages;
+          const int st = ig % Smem::kQStages;
+          const int use = ig / Smem::kQStages;
           const int g = it / un.n_qt;
           const int q0 = (un.qt_lo + it % un.n_qt) * kTileM;
           const int zq = un.bz * p.Hq + un.hk * p.group + g;
@@ -338,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*abort_flag) {
         if (uk > 0) mbar_drain(&s.kv_full, (uk - 1) & 1, kSiteDrain);
-        for (int i = max(0, issued - kQStages); i < issued; ++i)
-          mbar_drain(&s.q_full[i % kQStages], (i / kQStages) & 1, kSiteDrain);
+        for (int i = max(0, issued - Smem::kQStages); i < issued; ++i)
+          mbar_drain(&s.q_full[i % Smem::kQStages], (i / Smem::kQStages) & 1, kSiteDrain);
         if (do_issued > 0) mbar_drain(&s.do_full, (do_issued - 1) & 1, kSiteDrain);
       }
     }
@@ -375,13 +376,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!un.exists || un.n_it == 0) continue;
         if (!mbar_wait_warp(&s.kv_full, uk & 1, abort_flag, kSiteKV)) break;
         for (int it = 0; ok && it < un.n_it; ++it, ++ig) {
-          const int st = ig % kQStages;
+          const int st = ig % Smem::kQStages;
           const uint32_t so = static_cast<uint32_t>(st) * kStage;
           // Q and dO arrive by TMA (the mbarrier wait orders them before the
           // MMAs); the S^T columns this overwrites were last touched by other
           // threads before p_full of the previous tile, whose fence covers them.
           if (it == 0) {
-            if (!mbar_wait_warp(&s.q_full[st], (ig / kQStages) & 1, abort_flag, kSiteQFull)) {
+            if (!mbar_wait_warp(&s.q_full[st], (ig / Smem::kQStages) & 1, abort_flag, kSiteQFull)) {
               ok = false;
               break;
             }
@@ -425,9 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_warp(&s.do_empty);  // dO has been read: the next tile's may load
           // next tile's S^T now: the pipe runs dV before it, so P^T has been read
           if (it + 1 < un.n_it) {
-            const int st1 = (ig + 1) % kQStages;
+            const int st1 = (ig + 1) % Smem::kQStages;
             const uint32_t so1 = static_cast<uint32_t>(st1) * kStage;
-            if (!mbar_wait_warp(&s.q_full[st1], ((ig + 1) / kQStages) & 1, abort_flag, kSiteQFull)) {
+            if (!mbar_wait_warp(&s.q_full[st1], ((ig + 1) / Smem::kQStages) & 1, abort_flag, kSiteQFull)) {
               ok = false;
               break;
             }

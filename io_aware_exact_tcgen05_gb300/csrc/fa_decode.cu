@@ -32,8 +32,8 @@ namespace {
 
 constexpr int kComputeWarps = 8;
 constexpr int kThreads = (kComputeWarps + 1) * 32;  // + 1 producer warp
-constexpr int kStageKeys = 128;
-constexpr int kStages = 3;
+constexpr int kStageKeys = DecodeTiles::kStageKeys;
+constexpr int kStages = DecodeTiles::kStages;
 constexpr int kMaxHeadsPerCta = 8;
 
 enum : unsigned int { kSiteFull = 1, kSiteEmpty = 2, kSiteDrain = 3 };
@@ -432,7 +432,7 @@ void decode_plan(int B, int Hq, int Hkv, int Sk_max, int* chunk, int* n_split) {
   // reached 4.1 TB/s, 4096-key chunks 6.1 TB/s); short caches use smaller
   // chunks so that a row still spreads over several CTAs.  Multiple of the
   // 128-key stage.
-  int c = 4096;
+  int c = DecodeTiles::kMaxChunk;
   while (c > kStageKeys && Sk_max <= 4 * c) c >>= 1;
   *chunk = c;
   *n_split = (Sk_max + c - 1) / c;

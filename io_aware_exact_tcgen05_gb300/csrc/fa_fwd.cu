@@ -58,7 +58,7 @@ enum : unsigned int {
 template <int D>
 struct FwdSmem {
   static constexpr int NB = D / 64;               // 64-wide (128-byte) column blocks per row
-  static constexpr int NS = (D == 128) ? 2 : 3;   // K and V pipeline depth
+  static constexpr int NS = FwdTiles<D>::kKvStages;  // K and V pipeline depth
   static constexpr int kBox = kTileM * 64;        // elements per 128-row x 64-col box
   __nv_bfloat16 q[2][NB][kBox];
   __nv_bfloat16 k[NS][NB][kBox];

@@ -39,7 +39,7 @@ namespace {
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kD = 128;                   // head dimension (bytes per fp8 row)
-constexpr int kNS = 3;                    // K and V^T pipeline depth
+constexpr int kNS = Fp8Tiles::kKvStages;  // K and V^T pipeline depth
 constexpr uint32_t kTile = 128 * 128;     // bytes of one 128 x 128 e4m3 tile
 constexpr float kFastLimitFp8 = 448.f;    // e4m3's largest finite value
 

@@ -26,10 +26,39 @@ inline void hook_after(cudaStream_t s) {
   profile_hook() = ProfileHook{};
 }
 
+// ---------------------------------------------------------------------------
+// Tile-size and pipeline table.  Every tile shape, pipeline depth and split
+// length of the kernels is read from here, per head dimension and kernel;
+// each value is the one measured fastest on GB300 among the alternatives
+// that fit the 227 KB of shared memory per CTA (and 512 TMEM columns).
+// ---------------------------------------------------------------------------
+
 // Rows of one query tile and keys of one key/value tile in the tensor-core
-// kernels (one tcgen05.mma M=128 accumulator; 128 TMEM lanes).
+// kernels (one tcgen05.mma M=128 accumulator; 128 TMEM lanes).  Two query
+// tiles ("slots") share each K/V tile in the forward: two S tiles and two O
+// accumulators fill the 512 TMEM columns at d = 128.
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
+
+// bf16 forward: K/V pipeline depth (stages of one 128-key K tile and V tile).
+template <int D> struct FwdTiles;
+template <> struct FwdTiles<128> { static constexpr int kKvStages = 2; };  // 3 needs 256 KB
+template <> struct FwdTiles<64> { static constexpr int kKvStages = 3; };
+
+// Backward main kernel: Q tile buffers (S^T(i+1) is issued before dK(i) has
+// read Q(i), so two are needed); dO has one buffer.
+template <int D> struct BwdTiles { static constexpr int kQStages = 2; };
+
+// FP8 forward (d = 128): K / V^T pipeline depth.
+struct Fp8Tiles { static constexpr int kKvStages = 3; };
+
+// Decode: keys per pipeline stage, stages per CTA, and the longest split a
+// CTA streams (shorter caches use shorter splits, see decode_plan).
+struct DecodeTiles {
+  static constexpr int kStageKeys = 128;
+  static constexpr int kStages = 3;
+  static constexpr int kMaxChunk = 4096;
+};
 
 // Dropout on the attention weights (see fa_philox.cuh for the mapping).
 struct DropoutArgs {
