@@ -116,15 +116,12 @@ __device__ __forceinline__ void mask_key_bits(uint32_t (&sr)[kTileN], uint4 kb) 
 // from t_p.  sum2 gathers the fp32 weights (for l); sr_lo/sr_hi gather the
 // rounded ones (for lr).  With DROP, the stored words of dropped weights are
 // cleared after the sums (l, lr and the LSE stay those of the undropped
-// softmax); key8 is the tile's first key / 8, row and bh the Philox counter's
-// query row and query head.
+// softmax); bit jj of keep[jj / 32] says whether key jj of the tile is kept.
 template <int HALF, bool DROP>
 __device__ __forceinline__ void softmax_half(const uint32_t (&sr)[kTileN], uint64_t c2,
                                              uint64_t nmc2, uint32_t t_p, uint64_t (&sum2)[4],
                                              float (&sr_lo)[4], float (&sr_hi)[4],
-                                             const DropoutArgs& drop, uint32_t key8, uint32_t row,
-                                             uint32_t bh) {
-  uint32_t keep8 = 0;
+                                             const uint32_t (&keep)[4]) {
   uint32_t pk[kTileN / 4];
 #pragma unroll
   for (int jq = 0; jq < kTileN / 4; ++jq) {
@@ -139,8 +136,8 @@ __device__ __forceinline__ void softmax_half(const uint32_t (&sr)[kTileN], uint6
     sum2[jq & 3] = f2_add(sum2[jq & 3], f2_pack(p0, p1));
     add_bf16x2_f32(sr_lo[jq & 3], sr_hi[jq & 3], pk[jq]);
     if (DROP) {
-      if ((jq & 3) == 0) keep8 = dropout_keep8(drop, key8 + HALF * 8 + jq / 4, row, bh);
-      const uint32_t kb = keep8 >> (2 * (jq & 3));
+      const int kj = HALF * (kTileN / 2) + 2 * jq;  // the pair's first key in the tile
+      const uint32_t kb = keep[kj >> 5] >> (kj & 31);
       pk[jq] &= ((kb & 1u) ? 0x0000ffffu : 0u) | ((kb & 2u) ? 0xffff0000u : 0u);
     }
   }
@@ -446,6 +443,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = neg_inf();  // running max of raw scores (unscaled)
       float l = 0.f;        // running denominator, relative to 2^(m*c)
       float lr = 0.f;       // same, over the bf16-rounded weights
+      // Dropout keep bits of this row for one key tile (bit jj of word jj / 32
+      // = key jj of the tile kept).  They are computed one tile ahead, after
+      // the row's P has been released and while the warp waits for the next
+      // S, so the Philox rounds stay off the S -> P path.
+      uint32_t keep[4] = {~0u, ~0u, ~0u, ~0u};
+      auto keep_bits = [&](int jt) {
+        const uint32_t k8 = static_cast<uint32_t>((j0 + jt) * kTileN) >> 3;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            word |= dropout_keep8(p.drop, k8 + 4 * w + g, static_cast<uint32_t>(i), bh) << (8 * g);
+          keep[w] = word;
+        }
+      };
+      if (DROP && n_tiles > 0) keep_bits(0);
       for (int j = 0; j < n_tiles; ++j) {
         if (!mbar_wait_warp(&s.s_full[t], (ts + j) & 1, abort_flag, kSiteSFull)) {
           ok = false;
@@ -458,7 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
         tmem_wait_ld();
         const int c0 = (j0 + j) * kTileN;
-        const uint32_t key8 = static_cast<uint32_t>(c0) >> 3;  // dropout counter word 0
         const bool need_mask = (c0 < klo) || (c0 + kTileN > khi_row);
         const bool masked_tile = __any_sync(0xffffffffu, need_mask);
         if (masked_tile) mask_scores<0, kTileN>(sr, c0, klo, khi_row);
@@ -480,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!exact) {
           const float mc = m * c;
           const uint64_t nmc2 = f2_pack(-mc, -mc);
-          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key8, i, bh);
-          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key8, i, bh);
+          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, keep);
+          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, keep);
           const float ts = sum_f2x4(sum2);
           exact = __any_sync(0xffffffffu, !(ts < kFastLimit));
           if (!exact) {
@@ -537,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             sr_lo[q2] = 0.f;
             sr_hi[q2] = 0.f;
           }
-          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key8, i, bh);
-          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, p.drop, key8, i, bh);
+          softmax_half<0, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, keep);
+          softmax_half<1, DROP>(sr, c2, nmc2, t_p, sum2, sr_lo, sr_hi, keep);
           l += sum_f2x4(sum2);
           lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
                 ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
@@ -561,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.p_full[t]);
+        if (DROP && j + 1 < n_tiles) keep_bits(j + 1);
       }
       if (!ok) break;
       if (n_tiles > 0) {
