@@ -598,11 +598,9 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
   const double qk = static_cast<double>(scale) * q_descale * k_descale;
   p.scale_qk = static_cast<float>(qk);
   p.scale_log2 = scale_log2_of(static_cast<float>(qk));
-  // e4m3 tops out at 448: a redo keeps every weight of the row <= 2, so a
-  // tile's weight sum (<= 256) stays inside the fast path's bound afterwards
-  // (with a larger threshold the later tiles of a row whose max grew would
-  // each fail it and be computed twice)
-  p.rescale_log2 = 1.0f;
+  // e4m3 tops out at 448: the running max moves once the tile max exceeds
+  // it by more than 2^8, so every weight stays <= 256
+  p.rescale_log2 = 8.0f;
   p.v_descale = v_descale;
   if (1LL * p.n_rbu * p.units_per_rbu >= (1LL << 31))
     return fail(FA_ERR_INVALID_ARG, "grid too large");

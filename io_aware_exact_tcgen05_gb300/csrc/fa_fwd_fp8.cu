@@ -7,22 +7,21 @@
 //
 //   S_t = Q_t K_j^T     tcgen05.mma kind::f8f6f4, e4m3 A (Q) and B (K) from
 //                       shared memory, fp32 in TMEM; K = 32 per instruction
-//   P_t                 softmax warps: weights as in the bf16 forward, rounded
-//                       to e4m3 (saturating at 448) and written row by row to
-//                       shared memory in the MMA's K-major 128-byte-swizzled
-//                       layout
-//   O_t += P_t V_j      tcgen05.mma kind::f8f6f4, A = P (shared), B = V^T
+//   P_t                 softmax warps: the tile's row max, weights against
+//                       the lazily moved running max, rounded to e4m3 and
+//                       stored into the last 32 TMEM columns of S_t (four
+//                       weights per column)
+//   O_t += P_t V_j      tcgen05.mma kind::f8f6f4, A = P (TMEM), B = V^T
 //                       (shared; V is passed transposed, [d, Sk] per head, so
-//                       that both operands of both products are K-major)
+//                       that B is K-major like K)
 //
 // Dequantisation is folded into the arithmetic: the score scale becomes
 // scale * q_descale * k_descale, and O is multiplied by v_descale once in the
-// epilogue.  Weights are kept below 448 (e4m3's largest finite value): the
-// fast path accepts a tile only while the row's fp32 weight sum stays below
-// it, and the exact path rescales once the max grows by more than 2^1, so
-// that later tiles of the row pass that bound again.  O is
-// divided by the sum of the *rounded* weights (what the PV product used), l
-// (fp32, unrounded) gives the LSE.
+// epilogue.  Weights are kept below 448 (e4m3's largest finite value): every
+// tile's row max is taken, and the running max moves (rescaling l and O)
+// once the tile max exceeds it by more than 2^8, so no weight exceeds 256.
+// O is divided by the sum of the *rounded* weights (what the PV product
+// used), l (fp32, unrounded) gives the LSE.
 //
 // Method: as fa_fwd.cu ("Flash Attention" history page 1.2, 1.3, 2.1, 2.3;
 // FlashAttention_01 page, online-softmax derivation and masking rule).
@@ -41,7 +40,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kD = 128;                   // head dimension (bytes per fp8 row)
 constexpr int kNS = Fp8Tiles::kKvStages;  // K and V^T pipeline depth
 constexpr uint32_t kTile = 128 * 128;     // bytes of one 128 x 128 e4m3 tile
-constexpr float kFastLimitFp8 = 448.f;    // e4m3's largest finite value
 
 enum : unsigned int {
   kSiteQ = 1, kSiteKFree, kSiteVFree, kSiteKFull, kSiteVFull, kSitePFull, kSiteSFull,
@@ -52,7 +50,6 @@ struct Fp8Smem {
   uint8_t q[2][kTile];      // Q_t, rows = query rows, 128 bytes (= d) per row
   uint8_t k[kNS][kTile];    // K_j, rows = keys
   uint8_t vt[kNS][kTile];   // V_j^T, rows = head dimension, 128 keys per row
-  uint8_t p[2][kTile];      // P_t, rows = query rows, 128 keys per row
   uint64_t bar_q;
   uint64_t k_full[kNS], v_full[kNS];
   uint64_t kv_free[kNS];    // round i read K tile i and V tile i - 1
@@ -63,13 +60,6 @@ struct Fp8Smem {
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
 
 __device__ __forceinline__ void mask_scores(uint32_t (&sr)[kTileN], int first, int count, int c0,
                                             int klo, int khi) {
@@ -82,22 +72,22 @@ __device__ __forceinline__ void mask_scores(uint32_t (&sr)[kTileN], int first, i
 }
 
 // Weights 2^(s*c - mc) of the tile's 128 scores (nmc2 holds -mc twice),
-// rounded to e4m3 and written as the row's 128 bytes of P (eight swizzled
-// 16-byte chunks); sum2 gathers the fp32 weights (l), sr_lo/sr_hi the rounded
-// ones (lr).
+// rounded to e4m3 and stored as the row's 128 bytes of P in TMEM (32
+// columns from t_p, four keys per column, key 4w + b in byte b of column w);
+// sum2 gathers the fp32 weights (l), sr_lo/sr_hi the rounded ones (lr).
 __device__ __forceinline__ void softmax_tile_fp8(const uint32_t (&sr)[kTileN], uint64_t c2,
-                                                 uint64_t nmc2, uint32_t p_row, int row,
+                                                 uint64_t nmc2, uint32_t t_p,
                                                  uint64_t (&sum2)[4], float (&sr_lo)[4],
                                                  float (&sr_hi)[4]) {
 #pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {  // 16 keys per chunk
-    uint32_t w[4];
+  for (int hf = 0; hf < 2; ++hf) {  // 64 keys, 16 columns per store
+    uint32_t w[16];
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {  // 4 keys per 32-bit word
+    for (int q4 = 0; q4 < 16; ++q4) {  // 4 keys per 32-bit word
       uint16_t h[2];
 #pragma unroll
       for (int pr = 0; pr < 2; ++pr) {
-        const int jj = ch * 16 + q4 * 4 + pr * 2;
+        const int jj = hf * 64 + q4 * 4 + pr * 2;
         float x0, x1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[jj]), __uint_as_float(sr[jj + 1])), c2, nmc2),
                   x0, x1);
@@ -110,7 +100,7 @@ __device__ __forceinline__ void softmax_tile_fp8(const uint32_t (&sr)[kTileN], u
       }
       w[q4] = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
     }
-    st_shared_v4(p_row + ((ch ^ (row & 7)) * 16), w[0], w[1], w[2], w[3]);
+    tmem_st16(t_p + hf * 16, w);
   }
 }
 
@@ -235,8 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qd1 = smem_desc_sw128(smem_u32(s.q[1]), 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
       const uint64_t vd0 = smem_desc_sw128(smem_u32(s.vt[0]), 16, 1024);
-      const uint64_t pd0 = smem_desc_sw128(smem_u32(s.p[0]), 16, 1024);
-      const uint64_t pd1 = smem_desc_sw128(smem_u32(s.p[1]), 16, 1024);
       bool ok = mbar_wait_warp(&s.bar_q, 0, abort_flag, kSiteQ);
       tc_fence_after();
       for (int j = 0; ok && j <= n_tiles; ++j) {
@@ -247,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < nslots; ++t) {
           const uint32_t t_s = tmem + t * kTileN;
           if (j > 0) {
-            // O_t += P_t(j-1) V_{j-1}: P from shared memory (generic-proxy
-            // stores fenced to the async proxy before p_full), V^T from TMA
+            // O_t += P_t(j-1) V_{j-1}: P from TMEM (the softmax warps' stores
+            // ordered before p_full by the tcgen05 fences), V^T from TMA
             if (!mbar_wait_warp(&s.p_full[t], (j - 1) & 1, abort_flag, kSitePFull)) {
               ok = false;
               break;
@@ -260,10 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();  // the softmax warps' TMEM reads of S_t come first
             const uint32_t t_o = tmem + 2 * kTileN + t * kD;
-            const uint64_t pd = t ? pd1 : pd0;
+            // P_t lives in the last 32 columns of S_t
+            const uint32_t t_p = t_s + kTileN - kTileN / 4;
 #pragma unroll
             for (int kk = 0; kk < kTileN / 32; ++kk)
-              mma_ss_warp_f8(t_o, desc_add(pd, kk * 32), desc_add(vd, kk * 32), idesc,
+              mma_ts_warp_f8(t_o, t_p + kk * 8, desc_add(vd, kk * 32), idesc,
                              (j > 1 || kk > 0) ? 1u : 0u);
           }
           if (j < n_tiles) {
@@ -294,8 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + t * kTileN + lane_off;
     const uint32_t t_o = tmem + 2 * kTileN + t * kD + lane_off;
-    // this row's 128 bytes of P: 8-row swizzle atoms of 1024 bytes
-    const uint32_t p_row = smem_u32(s.p[t]) + static_cast<uint32_t>(row_in_tile) * 128;
+    // this row's 128 bytes of P: the last 32 TMEM columns of S_t (the
+    // scores are all in registers by then)
+    const uint32_t t_p = t_s + kTileN - kTileN / 4;
     const float c = p.scale_log2;
     int khi_row = kend;
     if (p.causal) khi_row = min(khi_row, i + off + 1);
@@ -315,53 +305,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c0 = (j0 + j) * kTileN;
         const bool need_mask = (c0 < klo) || (c0 + kTileN > khi_row);
         if (__any_sync(0xffffffffu, need_mask)) mask_scores(sr, 0, kTileN, c0, klo, khi_row);
-        // fast path against the running max; exact path when a row has no
-        // max yet or a weight could exceed e4m3's range
-        bool exact = __any_sync(0xffffffffu, m == neg_inf());
+        // Row max of the tile, then the lazily moved running max: m moves to
+        // the new max only when that grows by more than 2^rescale_log2 (= 2^8),
+        // so every weight 2^(s*c - m*c) stays at most 256, inside e4m3's range
+        // (448).  A row's first visible key always sets m; the difference
+        // m_new - m is formed only once m is finite (no -inf - (-inf)).
+        float mx8[8];
+#pragma unroll
+        for (int q2 = 0; q2 < 8; ++q2)
+          mx8[q2] = fmaxf(__uint_as_float(sr[q2]), __uint_as_float(sr[q2 + 8]));
+#pragma unroll
+        for (int jj = 16; jj < kTileN; jj += 16)
+#pragma unroll
+          for (int q2 = 0; q2 < 8; ++q2)
+            mx8[q2] = max3f(mx8[q2], __uint_as_float(sr[jj + q2]), __uint_as_float(sr[jj + 8 + q2]));
+        const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
+        const float m_new = fmaxf(m, mx);
+        const bool first = (m == neg_inf()) && (m_new != neg_inf());
+        const bool grow = first || (m != neg_inf() && (m_new - m) * c > p.rescale_log2);
+        const float alpha = first ? 0.f : (grow ? ex2_approx((m - m_new) * c) : 1.f);
+        if (grow) {
+          l *= alpha;
+          lr *= alpha;
+          m = m_new;
+        }
+        const float mc = (m == neg_inf()) ? 0.f : m * c;
         const uint64_t c2 = f2_pack(c, c);
         uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
         float sr_lo[4] = {0.f, 0.f, 0.f, 0.f}, sr_hi[4] = {0.f, 0.f, 0.f, 0.f};
-        if (!exact) {
-          const float mc = m * c;
-          softmax_tile_fp8(sr, c2, f2_pack(-mc, -mc), p_row, row_in_tile, sum2, sr_lo, sr_hi);
-          const float ts = sum_f2x4(sum2);
-          exact = __any_sync(0xffffffffu, !(ts < kFastLimitFp8));
-          if (!exact) {
-            l += ts;
-            lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
-                  ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
-          }
-        }
-        bool grow = false;
-        float alpha = 1.f;
-        if (exact) {
-          // the scores are still in registers (P went to shared memory)
-          float mx = neg_inf();
-#pragma unroll
-          for (int jj = 0; jj < kTileN; jj += 2)
-            mx = max3f(mx, __uint_as_float(sr[jj]), __uint_as_float(sr[jj + 1]));
-          const float m_new = fmaxf(m, mx);
-          // the difference is formed only once m is finite (no -inf - (-inf))
-          const bool first = (m == neg_inf()) && (m_new != neg_inf());
-          grow = first || (m != neg_inf() && (m_new - m) * c > p.rescale_log2);
-          alpha = first ? 0.f : (grow ? ex2_approx((m - m_new) * c) : 1.f);
-          if (grow) {
-            l *= alpha;
-            lr *= alpha;
-            m = m_new;
-          }
-          const float mc = (m == neg_inf()) ? 0.f : m * c;
-#pragma unroll
-          for (int q2 = 0; q2 < 4; ++q2) {
-            sum2[q2] = 0ull;
-            sr_lo[q2] = 0.f;
-            sr_hi[q2] = 0.f;
-          }
-          softmax_tile_fp8(sr, c2, f2_pack(-mc, -mc), p_row, row_in_tile, sum2, sr_lo, sr_hi);
-          l += sum_f2x4(sum2);
-          lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
-                ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
-        }
+        softmax_tile_fp8(sr, c2, f2_pack(-mc, -mc), t_p, sum2, sr_lo, sr_hi);
+        l += sum_f2x4(sum2);
+        lr += (sr_lo[0] + sr_lo[1]) + (sr_lo[2] + sr_lo[3]) +
+              ((sr_hi[0] + sr_hi[1]) + (sr_hi[2] + sr_hi[3]));
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
           // O_t is quiescent: PV_t(j-1) completed before S_t(j) was signalled
 #pragma unroll
@@ -376,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // P (generic stores) must be visible to the MMA's async-proxy reads;
-        // the S loads and any O rescale are ordered by the tcgen05 fence
-        fence_proxy_async_smem();
+        // the S loads, the P stores and any O rescale are ordered before the
+        // next MMAs by the tcgen05 fence
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.p_full[t]);

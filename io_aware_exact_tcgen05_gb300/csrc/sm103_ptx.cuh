@@ -275,6 +275,19 @@ __device__ __forceinline__ void mma_ss_warp_f8(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
+// kind::f8f6f4 form of mma_ts_warp: A (8-bit, four values per 32-bit TMEM
+// column, 32 values = 8 columns per instruction) from TMEM.
+__device__ __forceinline__ void mma_ts_warp_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
