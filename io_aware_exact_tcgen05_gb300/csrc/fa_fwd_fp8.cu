@@ -7,24 +7,27 @@
 //
 //   S_t = Q_t K_j^T     tcgen05.mma kind::f8f6f4, e4m3 A (Q) and B (K) from
 //                       shared memory, fp32 in TMEM; K = 32 per instruction
-//   P_t                 softmax warps: the tile's row max, weights against
-//                       the lazily moved running max, rounded to e4m3 and
-//                       stored into the last 32 TMEM columns of S_t (four
-//                       weights per column)
-//   O_t += P_t V_j      tcgen05.mma kind::f8f6f4, A = P (TMEM), B = V^T
+//   P_t                 softmax warps: weights as in the bf16 forward, rounded
+//                       to e4m3 (saturating at 448) and written row by row to
+//                       shared memory in the MMA's K-major 128-byte-swizzled
+//                       layout
+//   O_t += P_t V_j      tcgen05.mma kind::f8f6f4, A = P (shared), B = V^T
 //                       (shared; V is passed transposed, [d, Sk] per head, so
-//                       that B is K-major like K)
+//                       that both operands of both products are K-major)
 //
 // Dequantisation is folded into the arithmetic: the score scale becomes
 // scale * q_descale * k_descale, and O is multiplied by v_descale once in the
-// epilogue.  Weights are kept below 448 (e4m3's largest finite value): every
-// tile's row max is taken, and the running max moves (rescaling l and O)
-// once the tile max exceeds it by more than 2^8, so no weight exceeds 256.
-// O is divided by the sum of the *rounded* weights (what the PV product
-// used), l (fp32, unrounded) gives the LSE.
+// epilogue.  Weights are kept below 448 (e4m3's largest finite value): the
+// fast path accepts a tile only while the row's fp32 weight sum stays below
+// it, and the exact path rescales once the max grows by more than 2^1, so
+// that later tiles of the row pass that bound again.  O is
+// divided by the sum of the *rounded* weights (what the PV product used), l
+// (fp32, unrounded) gives the LSE.
 //
 // Method: as fa_fwd.cu ("Flash Attention" history page 1.2, 1.3, 2.1, 2.3;
 // FlashAttention_01 page, online-softmax derivation and masking rule).
+#include <algorithm>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -51,9 +54,11 @@ struct Fp8Smem {
   uint8_t k[kNS][kTile];    // K_j, rows = keys
   uint8_t vt[kNS][kTile];   // V_j^T, rows = head dimension, 128 keys per row
   uint64_t bar_q;
+  uint64_t q_free;          // the unit's last S product has read Q
   uint64_t k_full[kNS], v_full[kNS];
-  uint64_t kv_free[kNS];    // round i read K tile i and V tile i - 1
+  uint64_t kv_free[kNS];    // round g (tiles counted across units) read K tile g and V tile g - 1
   uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t o_empty[2];      // the slot's softmax warps have read O
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -110,6 +115,57 @@ __device__ __forceinline__ float sum_f2x4(const uint64_t (&v)[4]) {
   return a + b;
 }
 
+// One work unit: two 128-row query tiles (slots) and the key tiles they see,
+// numbered heavy (late) row blocks first, as in the bf16 forward.
+struct Fp8Unit {
+  int b, h0, h1, r0, r1;
+  bool active1;
+  int hk, klo, kend, off, j0, n_tiles;
+};
+
+__device__ __forceinline__ Fp8Unit fp8_unit_at(const Fp8FwdParams& p, int U) {
+  Fp8Unit u;
+  const int rbu = p.n_rbu - 1 - U / p.units_per_rbu;
+  const int w = U % p.units_per_rbu;
+  if (p.pack_heads) {
+    const int hpairs = p.Hq >> 1;
+    u.b = w / hpairs;
+    u.h0 = 2 * (w % hpairs);
+    u.h1 = u.h0 + 1;
+    u.r0 = u.r1 = rbu * kTileM;
+  } else {
+    u.b = w / p.Hq;
+    u.h0 = u.h1 = w % p.Hq;
+    u.r0 = rbu * 2 * kTileM;
+    u.r1 = u.r0 + kTileM;
+  }
+  u.active1 = u.r1 < p.Sq;
+  u.hk = u.h0 / p.group;
+  u.klo = p.k_start ? p.k_start[u.b] : 0;
+  u.kend = p.k_end ? p.k_end[u.b] : p.Sk;
+  u.klo = max(0, min(u.klo, p.Sk));
+  u.kend = max(0, min(u.kend, p.Sk));
+  u.off = p.Sk - p.Sq;  // bottom-right causal alignment
+  int khi = u.kend;
+  if (p.causal) {
+    const int last_row = min((u.active1 ? u.r1 : u.r0) + kTileM - 1, p.Sq - 1);
+    khi = min(khi, last_row + u.off + 1);
+  }
+  u.j0 = 0;
+  u.n_tiles = 0;
+  if (khi > u.klo) {
+    u.j0 = u.klo / kTileN;
+    u.n_tiles = (khi + kTileN - 1) / kTileN - u.j0;
+  }
+  return u;
+}
+
+// Persistent, like the bf16 forward: one CTA per SM walks the heavy-first
+// unit list in alternating directions block by block.  Barrier phases run on
+// across units: the next unit's Q is loaded once the current unit's last S
+// product has read Q (q_free), K/V stages and their release commits count
+// tiles across units, and the next unit's first PV into O_t waits only until
+// the softmax warps have read O_t in the epilogue (o_empty).
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tvt, const Fp8FwdParams p) {
@@ -118,44 +174,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work unit (as the bf16 forward): heavy row blocks first -----------
-  const int L = blockIdx.x;
-  const int rbu = p.n_rbu - 1 - L / p.units_per_rbu;
-  const int u = L % p.units_per_rbu;
-  int b, h0, h1, r0, r1;
-  if (p.pack_heads) {
-    const int hpairs = p.Hq >> 1;
-    b = u / hpairs;
-    h0 = 2 * (u % hpairs);
-    h1 = h0 + 1;
-    r0 = r1 = rbu * kTileM;
-  } else {
-    b = u / p.Hq;
-    h0 = h1 = u % p.Hq;
-    r0 = rbu * 2 * kTileM;
-    r1 = r0 + kTileM;
-  }
-  const bool active1 = r1 < p.Sq;
-  const int hk = h0 / p.group;
-  int klo = p.k_start ? p.k_start[b] : 0;
-  int kend = p.k_end ? p.k_end[b] : p.Sk;
-  klo = max(0, min(klo, p.Sk));
-  kend = max(0, min(kend, p.Sk));
-  const int off = p.Sk - p.Sq;  // bottom-right causal alignment
-  int khi = kend;
-  if (p.causal) {
-    const int last_row = min((active1 ? r1 : r0) + kTileM - 1, p.Sq - 1);
-    khi = min(khi, last_row + off + 1);
-  }
-  int j0 = 0, n_tiles = 0;
-  if (khi > klo) {
-    j0 = klo / kTileN;
-    n_tiles = (khi + kTileN - 1) / kTileN - j0;
-  }
+  const int n_units = p.n_rbu * p.units_per_rbu;
+  auto unit_index = [&](int k) {
+    const int G = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    return k * G + ((k & 1) ? (G - 1 - c) : c);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&s.bar_q, 1);
+    mbar_init(&s.q_free, 1);
     for (int i = 0; i < kNS; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.v_full[i], 1);
@@ -163,8 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s.s_full[t], 1);
-      mbar_init(&s.p_full[t], 4);  // one arrival per softmax warp
+      mbar_init(&s.p_full[t], 4);   // one arrival per softmax warp
       mbar_init(&s.o_full[t], 1);
+      mbar_init(&s.o_empty[t], 4);  // the slot's softmax warps have read O
     }
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
@@ -181,35 +210,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &s.abort_flag;
   if (warp == 8) {
     // ------------------------------------------------------ TMA producer --
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tvt);
       const uint64_t keep = policy_evict_last();
-      mbar_arrive_expect_tx(&s.bar_q, (active1 ? 2 : 1) * kTile);
-      tma_load_3d(s.q[0], &tq, &s.bar_q, 0, r0, b * p.Hq + h0);
-      if (active1) tma_load_3d(s.q[1], &tq, &s.bar_q, 0, r1, b * p.Hq + h1);
-      const int zkv = b * p.Hkv + hk;
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % kNS;
-        const int use = j / kNS;
-        const int c0 = (j0 + j) * kTileN;
-        if (use > 0 && !mbar_wait(&s.kv_free[st], (use - 1) & 1, abort_flag, kSiteKFree)) break;
-        mbar_arrive_expect_tx(&s.k_full[st], kTile);
-        tma_load_3d_hint(s.k[st], &tk, &s.k_full[st], 0, c0, zkv, keep);
-        k_issued = j + 1;
-        if (use > 0) {
-          const int r = j - kNS + 1;
-          if (!mbar_wait(&s.kv_free[r % kNS], (r / kNS) & 1, abort_flag, kSiteVFree)) break;
+      int g = 0, uq = 0, k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+        const int U = unit_index(k);
+        if (U >= n_units) continue;
+        const Fp8Unit un = fp8_unit_at(p, U);
+        if (un.n_tiles == 0) continue;
+        if (uq > 0 && !mbar_wait(&s.q_free, (uq - 1) & 1, abort_flag, kSiteQ)) break;
+        mbar_arrive_expect_tx(&s.bar_q, (un.active1 ? 2 : 1) * kTile);
+        tma_load_3d(s.q[0], &tq, &s.bar_q, 0, un.r0, un.b * p.Hq + un.h0);
+        if (un.active1) tma_load_3d(s.q[1], &tq, &s.bar_q, 0, un.r1, un.b * p.Hq + un.h1);
+        ++uq;
+        const int zkv = un.b * p.Hkv + un.hk;
+        for (int j = 0; j < un.n_tiles; ++j, ++g) {
+          const int st = g % kNS;
+          const int use = g / kNS;
+          const int c0 = (un.j0 + j) * kTileN;
+          // stage st last held tile g - NS: its K was freed in round g - NS,
+          // its V^T in round g - NS + 1
+          if (use > 0 && !mbar_wait(&s.kv_free[st], (use - 1) & 1, abort_flag, kSiteKFree)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&s.k_full[st], kTile);
+          tma_load_3d_hint(s.k[st], &tk, &s.k_full[st], 0, c0, zkv, keep);
+          k_issued = g + 1;
+          if (use > 0) {
+            const int r = g - kNS + 1;
+            if (!mbar_wait(&s.kv_free[r % kNS], (r / kNS) & 1, abort_flag, kSiteVFree)) {
+              ok = false;
+              break;
+            }
+          }
+          // V^T tile: keys [c0, c0 + 128) of every head-dimension row
+          mbar_arrive_expect_tx(&s.v_full[st], kTile);
+          tma_load_3d_hint(s.vt[st], &tvt, &s.v_full[st], c0, 0, zkv, keep);
+          v_issued = g + 1;
         }
-        // V^T tile: keys [c0, c0 + 128) of every head-dimension row
-        mbar_arrive_expect_tx(&s.v_full[st], kTile);
-        tma_load_3d_hint(s.vt[st], &tvt, &s.v_full[st], c0, 0, zkv, keep);
-        v_issued = j + 1;
       }
       if (*abort_flag) {
-        mbar_drain(&s.bar_q, 0, kSiteDrain);
+        if (uq > 0) mbar_drain(&s.bar_q, (uq - 1) & 1, kSiteDrain);
         for (int j = max(0, k_issued - kNS); j < k_issued; ++j)
           mbar_drain(&s.k_full[j % kNS], (j / kNS) & 1, kSiteDrain);
         for (int j = max(0, v_issued - kNS); j < v_issued; ++j)
@@ -218,44 +264,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------- MMA issuer --
-    if (n_tiles > 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kTileM, kTileN);  // N = keys or d, both 128
-      const int nslots = active1 ? 2 : 1;
-      const uint64_t qd0 = smem_desc_sw128(smem_u32(s.q[0]), 16, 1024);
-      const uint64_t qd1 = smem_desc_sw128(smem_u32(s.q[1]), 16, 1024);
-      const uint64_t kd0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
-      const uint64_t vd0 = smem_desc_sw128(smem_u32(s.vt[0]), 16, 1024);
-      bool ok = mbar_wait_warp(&s.bar_q, 0, abort_flag, kSiteQ);
-      tc_fence_after();
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles && !mbar_wait_warp(&s.k_full[j % kNS], (j / kNS) & 1, abort_flag, kSiteKFull))
+    // Per unit, round j issues PV_t(j-1) and S_t(j) for each active slot.
+    constexpr uint32_t idesc = idesc_e4m3_f32(kTileM, kTileN);  // N = keys or d, both 128
+    const uint64_t qd0 = smem_desc_sw128(smem_u32(s.q[0]), 16, 1024);
+    const uint64_t qd1 = smem_desc_sw128(smem_u32(s.q[1]), 16, 1024);
+    const uint64_t kd0 = smem_desc_sw128(smem_u32(s.k[0]), 16, 1024);
+    const uint64_t vd0 = smem_desc_sw128(smem_u32(s.vt[0]), 16, 1024);
+    int g = 0, uq = 0;
+    int ts[2] = {0, 0}, us[2] = {0, 0};  // per slot: tiles and units so far
+    bool ok = true;
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+      const int U = unit_index(k);
+      if (U >= n_units) continue;
+      const Fp8Unit un = fp8_unit_at(p, U);
+      if (un.n_tiles == 0) continue;
+      const int n = un.n_tiles;
+      const int nslots = un.active1 ? 2 : 1;
+      if (!mbar_wait_warp(&s.bar_q, uq & 1, abort_flag, kSiteQ)) break;
+      ++uq;
+      for (int j = 0; ok && j <= n; ++j) {
+        const int gk = g + j, gv = g + j - 1;  // this round's K tile, V tile
+        if (j < n && !mbar_wait_warp(&s.k_full[gk % kNS], (gk / kNS) & 1, abort_flag, kSiteKFull)) {
+          ok = false;
           break;
-        const uint64_t kd = desc_add(kd0, static_cast<uint32_t>(j % kNS) * kTile);
-        const uint64_t vd = desc_add(vd0, static_cast<uint32_t>((j + kNS - 1) % kNS) * kTile);
+        }
+        const uint64_t kd = desc_add(kd0, static_cast<uint32_t>(gk % kNS) * kTile);
+        const uint64_t vd = desc_add(vd0, static_cast<uint32_t>(((gv % kNS) + kNS) % kNS) * kTile);
         for (int t = 0; t < nslots; ++t) {
           const uint32_t t_s = tmem + t * kTileN;
           if (j > 0) {
-            // O_t += P_t(j-1) V_{j-1}: P from TMEM (the softmax warps' stores
-            // ordered before p_full by the tcgen05 fences), V^T from TMA
-            if (!mbar_wait_warp(&s.p_full[t], (j - 1) & 1, abort_flag, kSitePFull)) {
-              ok = false;
-              break;
-            }
-            const int vs = (j - 1) % kNS;
-            if (t == 0 && !mbar_wait_warp(&s.v_full[vs], ((j - 1) / kNS) & 1, abort_flag, kSiteVFull)) {
+            // O_t += P_t(j-1) V_{j-1}: P from shared memory (generic-proxy
+            // stores fenced to the async proxy before p_full), V^T from TMA
+            if (!mbar_wait_warp(&s.p_full[t], (ts[t] + j - 1) & 1, abort_flag, kSitePFull) ||
+                (t == 0 &&
+                 !mbar_wait_warp(&s.v_full[gv % kNS], (gv / kNS) & 1, abort_flag, kSiteVFull)) ||
+                (j == 1 && us[t] > 0 &&
+                 !mbar_wait_warp(&s.o_empty[t], (us[t] - 1) & 1, abort_flag, kSiteOFull))) {
               ok = false;
               break;
             }
             tc_fence_after();  // the softmax warps' TMEM reads of S_t come first
             const uint32_t t_o = tmem + 2 * kTileN + t * kD;
-            // P_t lives in the last 32 columns of S_t
             const uint32_t t_p = t_s + kTileN - kTileN / 4;
 #pragma unroll
             for (int kk = 0; kk < kTileN / 32; ++kk)
               mma_ts_warp_f8(t_o, t_p + kk * 8, desc_add(vd, kk * 32), idesc,
                              (j > 1 || kk > 0) ? 1u : 0u);
           }
-          if (j < n_tiles) {
+          if (j < n) {
             const uint64_t qd = t ? qd1 : qd0;
 #pragma unroll
             for (int kk = 0; kk < kD / 32; ++kk)
@@ -267,35 +323,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (j < n_tiles) mma_commit_warp(&s.kv_free[j % kNS]);
+        if (j < n) mma_commit_warp(&s.kv_free[gk % kNS]);
+        if (j == n - 1) mma_commit_warp(&s.q_free);  // the unit's last S has read Q
       }
-      if (warp_aborted(abort_flag)) {
-        mma_commit_warp(&s.drain);
-        mbar_drain(&s.drain, 0, kSiteDrain);
+      g += n;
+      for (int t = 0; t < nslots; ++t) {
+        ts[t] += n;
+        ++us[t];
       }
+    }
+    if (warp_aborted(abort_flag)) {
+      mma_commit_warp(&s.drain);
+      mbar_drain(&s.drain, 0, kSiteDrain);
     }
   } else {
     // ---------------------------------------------------- softmax warps --
     const int t = warp >> 2;
     const int row_in_tile = (warp & 3) * 32 + lane;
-    const int i = (t == 0 ? r0 : r1) + row_in_tile;
-    const int h = (t == 0) ? h0 : h1;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + t * kTileN + lane_off;
     const uint32_t t_o = tmem + 2 * kTileN + t * kD + lane_off;
-    // this row's 128 bytes of P: the last 32 TMEM columns of S_t (the
-    // scores are all in registers by then)
+    // this row's 128 bytes of P: 8-row swizzle atoms of 1024 bytes
     const uint32_t t_p = t_s + kTileN - kTileN / 4;
     const float c = p.scale_log2;
-    int khi_row = kend;
-    if (p.causal) khi_row = min(khi_row, i + off + 1);
-    float m = neg_inf();
-    float l = 0.f;   // fp32 weights
-    float lr = 0.f;  // e4m3-rounded weights
-    bool ok = (t == 0) || active1;
-    if (ok && n_tiles > 0) {
+    int ts = 0, us = 0;  // this slot's tiles and units so far
+    bool ok = true;
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_units; ++k) {
+      const int U = unit_index(k);
+      if (U >= n_units) continue;
+      const Fp8Unit un = fp8_unit_at(p, U);
+      if (t == 1 && !un.active1) continue;
+      const int n_tiles = un.n_tiles, j0 = un.j0, klo = un.klo, kend = un.kend;
+      const int i = (t == 0 ? un.r0 : un.r1) + row_in_tile;
+      const int h = (t == 0) ? un.h0 : un.h1;
+      int khi_row = kend;
+      if (p.causal) khi_row = min(khi_row, i + un.off + 1);
+      float m = neg_inf();
+      float l = 0.f;   // fp32 weights
+      float lr = 0.f;  // e4m3-rounded weights
       for (int j = 0; j < n_tiles; ++j) {
-        if (!mbar_wait_warp(&s.s_full[t], j & 1, abort_flag, kSiteSFull)) { ok = false; break; }
+        if (!mbar_wait_warp(&s.s_full[t], (ts + j) & 1, abort_flag, kSiteSFull)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[kTileN];
 #pragma unroll
@@ -352,46 +419,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // the S loads, the P stores and any O rescale are ordered before the
-        // next MMAs by the tcgen05 fence
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.p_full[t]);
       }
-      if (ok) ok = mbar_wait_warp(&s.o_full[t], 0, abort_flag, kSiteOFull);
-      tc_fence_after();
-    }
-    // ---- epilogue: O = v_descale * u / lr, LSE = m * scale_qk + ln l -------
-    if (((t == 0) || active1) && ok && !warp_aborted(abort_flag)) {
-      const bool live = l > 0.f;
-      const float inv = live ? p.v_descale / lr : 0.f;
-      const bool in_range = i < p.Sq;
-      const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Sq + i;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * kD;
-#pragma unroll 1
-      for (int cc = 0; cc < kD / 32; ++cc) {
-        uint32_t orr[32];
-        if (n_tiles > 0) {
-          tmem_ld32(t_o + cc * 32, orr);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int q2 = 0; q2 < 32; ++q2) orr[q2] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int q2 = 0; q2 < 16; ++q2)
-          pk[q2] = pack_bf16x2(__uint_as_float(orr[2 * q2]) * inv,
-                               __uint_as_float(orr[2 * q2 + 1]) * inv);
-        if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-          for (int q2 = 0; q2 < 4; ++q2)
-            dst[q2] = make_uint4(pk[4 * q2], pk[4 * q2 + 1], pk[4 * q2 + 2], pk[4 * q2 + 3]);
-        }
+      if (!ok) break;
+      if (n_tiles > 0) {
+        if (!mbar_wait_warp(&s.o_full[t], us & 1, abort_flag, kSiteOFull)) break;
+        tc_fence_after();
       }
-      if (in_range && p.lse) p.lse[row] = live ? fmaf(m, p.scale_qk, logf(l)) : neg_inf();
+      if (warp_aborted(abort_flag)) break;
+      // ---- epilogue: O = v_descale * u / lr, LSE = m * scale_qk + ln l -----
+      {
+        const bool live = l > 0.f;
+        const float inv = live ? p.v_descale / lr : 0.f;
+        const bool in_range = i < p.Sq;
+        const size_t row = (static_cast<size_t>(un.b) * p.Hq + h) * p.Sq + i;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * kD;
+#pragma unroll 1
+        for (int cc = 0; cc < kD / 32; ++cc) {
+          uint32_t orr[32];
+          if (n_tiles > 0) {
+            tmem_ld32(t_o + cc * 32, orr);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int q2 = 0; q2 < 32; ++q2) orr[q2] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int q2 = 0; q2 < 16; ++q2)
+            pk[q2] = pack_bf16x2(__uint_as_float(orr[2 * q2]) * inv,
+                                 __uint_as_float(orr[2 * q2 + 1]) * inv);
+          if (in_range) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2)
+              dst[q2] = make_uint4(pk[4 * q2], pk[4 * q2 + 1], pk[4 * q2 + 2], pk[4 * q2 + 3]);
+          }
+        }
+        if (in_range && p.lse) p.lse[row] = live ? fmaf(m, p.scale_qk, logf(l)) : neg_inf();
+      }
+      if (n_tiles > 0) {
+        // O_t has been read: the next unit's first PV may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.o_empty[t]);
+        ts += n_tiles;
+        ++us;
+      }
     }
   }
 
@@ -413,7 +490,13 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const C
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const unsigned int grid = static_cast<unsigned int>(p.n_rbu) * p.units_per_rbu;
+  // persistent: one CTA per SM over the heavy-first unit list
+  int dev = 0, n_sm = 0;
+  cudaError_t e2 = cudaGetDevice(&dev);
+  if (e2 == cudaSuccess) e2 = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e2 != cudaSuccess) return e2;
+  const long long units = static_cast<long long>(p.n_rbu) * p.units_per_rbu;
+  const unsigned int grid = static_cast<unsigned int>(std::min<long long>(units, n_sm));
   hook_before(stream);
   fa_fwd_fp8_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tvt, p);
   hook_after(stream);

@@ -50,7 +50,7 @@ template <> struct FwdTiles<64> { static constexpr int kKvStages = 3; };
 template <int D> struct BwdTiles { static constexpr int kQStages = 2; };
 
 // FP8 forward (d = 128): K / V^T pipeline depth.
-struct Fp8Tiles { static constexpr int kKvStages = 3; };
+struct Fp8Tiles { static constexpr int kKvStages = 4; };
 
 // Decode: keys per pipeline stage, stages per CTA, and the longest split a
 // CTA streams (shorter caches use shorter splits, see decode_plan).
