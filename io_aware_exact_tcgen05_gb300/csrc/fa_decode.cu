@@ -338,6 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kComputeWarps) __syncthreads();  // (A) for the producer warp
   __syncthreads();
   if (*abort_flag) return;
+  // the merge kernel may launch now (it waits for this grid's completion)
+  griddep_launch_dependents();
   // ---- merge the warps' states, write this split's normalised partial ----
   for (int idx = threadIdx.x; idx < n_heads * D; idx += kThreads) {
     const int h = idx / D;
@@ -374,6 +376,7 @@ __global__ void __launch_bounds__(D) fa_decode_merge(const DecodeParams p) {
   const int n_valid = min(p.n_split, (seqlen + p.chunk - 1) / p.chunk);
   const float* lse2 = p.part_lse + static_cast<size_t>(bh) * p.n_split;
   const float* po = p.part_o + static_cast<size_t>(bh) * p.n_split * D;
+  griddep_wait();  // the partial kernel's results are complete and visible
   float M = neg_inf();
   for (int sidx = 0; sidx < n_valid; ++sidx) M = fmaxf(M, lse2[sidx]);
   float wsum = 0.f, o = 0.f;
@@ -417,7 +420,21 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   else if (heads <= 4) e = launch_partial<D, 4>(p, 4, stream);
   else e = launch_partial<D, 8>(p, 8, stream);
   if (e != cudaSuccess) return e;
-  fa_decode_merge<D><<<p.B * p.Hq, D, 0, stream>>>(p);
+  // The merge is launched as a programmatic dependent of the partial kernel,
+  // so its launch overlaps the partial kernel's tail; it waits for the
+  // partial results on the device (griddep_wait).
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned int>(p.B * p.Hq));
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, fa_decode_merge<D>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -385,6 +385,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
          ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel in the stream is still running; griddep_wait() blocks
+// until that kernel has completed and its memory is visible.  The previous
+// kernel lets the dependent launch begin with griddep_launch_dependents()
+// (or, without it, when it exits).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- math helpers --
 
 // Packed pairs of fp32 (low word = first element) for the f32x2 FMA/add pipes.
