@@ -49,10 +49,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// bf16x2 word -> two floats (exact: a bf16 is the high half of an fp32)
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 template <int D>
 struct DecodeSmem {
   __nv_bfloat16 k[kStages][kStageKeys * D];
@@ -423,19 +419,8 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   // The merge is launched as a programmatic dependent of the partial kernel,
   // so its launch overlaps the partial kernel's tail; it waits for the
   // partial results on the device (griddep_wait).
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(static_cast<unsigned int>(p.B * p.Hq));
-  cfg.blockDim = dim3(D);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, fa_decode_merge<D>, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_dependent(fa_decode_merge<D>, static_cast<unsigned int>(p.B * p.Hq), D, 0, stream,
+                          p);
 }
 
 }  // namespace

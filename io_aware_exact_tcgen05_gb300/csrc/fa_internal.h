@@ -26,6 +26,29 @@ inline void hook_after(cudaStream_t s) {
   profile_hook() = ProfileHook{};
 }
 
+// Launch `kernel` as a programmatic dependent of the previous kernel in the
+// stream: its launch overlaps that kernel's tail.  A kernel launched this
+// way calls griddep_wait() before it touches memory the previous kernel may
+// still use.  (Used for the decode merge; on the forward and backward
+// kernels it measured -2% to +0.3%.)
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // Tile-size and pipeline table.  Every tile shape, pipeline depth and split
 // length of the kernels is read from here, per head dimension and kernel;
