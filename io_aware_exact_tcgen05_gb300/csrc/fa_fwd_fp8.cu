@@ -364,30 +364,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_tiles; ++j) {
         if (!mbar_wait_warp(&s.s_full[t], (ts + j) & 1, abort_flag, kSiteSFull)) { ok = false; break; }
         tc_fence_after();
+        // The reducing TMEM load returns each 32-column chunk's max with the
+        // scores; a tile that needs masking takes its max after the mask.
         uint32_t sr[kTileN];
+        float cmx[kTileN / 32];
 #pragma unroll
         for (int cc = 0; cc < kTileN / 32; ++cc)
-          tmem_ld32(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+          tmem_ld32_max(t_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]), cmx[cc]);
         tmem_wait_ld();
         const int c0 = (j0 + j) * kTileN;
         const bool need_mask = (c0 < klo) || (c0 + kTileN > khi_row);
-        if (__any_sync(0xffffffffu, need_mask)) mask_scores(sr, 0, kTileN, c0, klo, khi_row);
         // Row max of the tile, then the lazily moved running max: m moves to
         // the new max only when that grows by more than 2^rescale_log2 (= 2^8),
         // so every weight 2^(s*c - m*c) stays at most 256, inside e4m3's range
         // (448).  A row's first visible key always sets m; the difference
         // m_new - m is formed only once m is finite (no -inf - (-inf)).
-        float mx8[8];
-#pragma unroll
-        for (int q2 = 0; q2 < 8; ++q2)
-          mx8[q2] = fmaxf(__uint_as_float(sr[q2]), __uint_as_float(sr[q2 + 8]));
-#pragma unroll
-        for (int jj = 16; jj < kTileN; jj += 16)
+        float mx = fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3]));
+        if (__any_sync(0xffffffffu, need_mask)) {
+          mask_scores(sr, 0, kTileN, c0, klo, khi_row);
+          float mx8[8];
 #pragma unroll
           for (int q2 = 0; q2 < 8; ++q2)
-            mx8[q2] = max3f(mx8[q2], __uint_as_float(sr[jj + q2]), __uint_as_float(sr[jj + 8 + q2]));
-        const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
-                               fmaxf(mx8[6], mx8[7]));
+            mx8[q2] = fmaxf(__uint_as_float(sr[q2]), __uint_as_float(sr[q2 + 8]));
+#pragma unroll
+          for (int jj = 16; jj < kTileN; jj += 16)
+#pragma unroll
+            for (int q2 = 0; q2 < 8; ++q2)
+              mx8[q2] = max3f(mx8[q2], __uint_as_float(sr[jj + q2]), __uint_as_float(sr[jj + 8 + q2]));
+          mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                     fmaxf(mx8[6], mx8[7]));
+        }
         const float m_new = fmaxf(m, mx);
         const bool first = (m == neg_inf()) && (m_new != neg_inf());
         const bool grow = first || (m != neg_inf() && (m_new - m) * c > p.rescale_log2);
