@@ -284,6 +284,19 @@ fa_status fa_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
    clear != 0 the words are reset to 0 afterwards. */
 fa_status fa_device_status(unsigned int* code_out, int clear);
 
+/* Self-test of the bounded device waits behind FA_ERR_TIMEOUT.  Enqueues on
+   `stream` one small kernel whose two warps wait, with the helpers every
+   attention kernel uses, on barriers that nothing arrives on: the first
+   wait runs out after its 1 s limit, records the timeout at wait site 0x7e
+   in the device status word and raises the kernel's abort flag; the second
+   gives up on seeing the flag (no second record).  The kernel then returns
+   normally and the context stays usable.  result is a device array of two
+   unsigned ints (16-byte aligned), set to 1 for each wait that reported
+   failure.  Afterwards fa_device_status() returns FA_ERR_TIMEOUT with the
+   word 0x007e0001.  Takes about one second; for tests of the failure path
+   only. */
+fa_status fa_selftest_wait_timeout(unsigned int* result, cudaStream_t stream);
+
 /* Profiling hook (the pages ask that a timing confirm which kernel actually
    ran).  start/stop are cudaEvent_t handles created by the caller.  The next
    fa_fwd, fa_bwd or fa_decode call made on this host thread records `start`

@@ -27,7 +27,7 @@ FA_ERR_TIMEOUT = 5
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_decode", "fa_decode_workspace_size",
             "fa_decode_noalloc", "fa_fwd_masked", "fa_bwd_masked", "fa_fwd_varlen",
             "fa_bwd_varlen", "fa_fwd_dropout", "fa_bwd_dropout", "fa_key_mask_words",
-            "fa_pack_key_mask", "fa_fwd_fp8", "fa_device_status",
+            "fa_pack_key_mask", "fa_fwd_fp8", "fa_device_status", "fa_selftest_wait_timeout",
             "fa_profile_next_launch", "fa_status_string", "fa_last_error_detail", "fa_version")
 
 _lib = None
@@ -80,6 +80,8 @@ def load_library(path: str = LIB_PATH):
     lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
     for f in (lib.fa_fwd, lib.fa_bwd, lib.fa_decode, lib.fa_device_status):
         f.restype = I
+    lib.fa_selftest_wait_timeout.argtypes = [P, P]
+    lib.fa_selftest_wait_timeout.restype = I
     lib.fa_profile_next_launch.argtypes = [P, P]
     lib.fa_profile_next_launch.restype = I
     lib.fa_status_string.argtypes = [I]
@@ -381,6 +383,16 @@ def fa_device_status(clear: bool = True):
     w = ctypes.c_uint(0)
     st = lib.fa_device_status(ctypes.byref(w), int(bool(clear)))
     return st, w.value
+
+
+def fa_selftest_wait_timeout(stream=None):
+    """Run the bounded-wait self-test (about 1 s): returns the two flags the
+    kernel sets (1 = that wait reported failure).  fa_device_status() then
+    reports the recorded timeout."""
+    lib = load_library()
+    res = torch.zeros(4, dtype=torch.int32, device="cuda")
+    _check(lib.fa_selftest_wait_timeout(_ptr(res), _stream(stream)), "fa_selftest_wait_timeout")
+    return [int(x) for x in res[:2].cpu()]
 
 
 def fa_profile_next_launch(start=None, stop=None):

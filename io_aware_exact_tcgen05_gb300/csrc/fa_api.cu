@@ -633,9 +633,18 @@ fa_status fa_device_status(unsigned int* code_out, int clear) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
   const unsigned int w = fa::read_fwd_status(clear != 0) | fa::read_decode_status(clear != 0) |
-                         fa::read_bwd_status(clear != 0) | fa::read_fwd_fp8_status(clear != 0);
+                         fa::read_bwd_status(clear != 0) | fa::read_fwd_fp8_status(clear != 0) |
+                         fa::read_selftest_status(clear != 0);
   if (code_out) *code_out = w;
   if (w != 0) return fail(FA_ERR_TIMEOUT, "device status word 0x%08x", w);
+  return ok();
+}
+
+fa_status fa_selftest_wait_timeout(unsigned int* result, cudaStream_t stream) {
+  FA_TRY(check_ptr(result, "result"));
+  FA_TRY(check_device());
+  const cudaError_t e = fa::launch_selftest_wait(result, stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -147,6 +147,11 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const Fp8FwdParams& p, cudaStream_t stream);
 unsigned int read_fwd_fp8_status(bool clear);
 
+// Self-test of the bounded waits (fa_selftest.cu): result[0], result[1] are
+// set to 1 when the two waits report failure.
+cudaError_t launch_selftest_wait(unsigned int* result, cudaStream_t stream);
+unsigned int read_selftest_status(bool clear);
+
 struct DecodeParams {
   const void* q;        // bf16 [B,Hq,1,d]
   const void* k;        // bf16 [B,Hkv,Sk_max,d]
