@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < nslots; ++t) {
           const uint32_t t_s = tmem + t * kTileN;
           if (j > 0) {
-            // O_t += P_t(j-1) V_{j-1}: P from shared memory (generic-proxy
-            // stores fenced to the async proxy before p_full), V^T from TMA
+            // O_t += P_t(j-1) V_{j-1}: P from TMEM (the softmax warps' stores
+            // ordered before p_full by the tcgen05 fences), V^T from TMA
             if (!mbar_wait_warp(&s.p_full[t], (ts[t] + j - 1) & 1, abort_flag, kSitePFull) ||
                 (t == 0 &&
                  !mbar_wait_warp(&s.v_full[gv % kNS], (gv / kNS) & 1, abort_flag, kSiteVFull)) ||
