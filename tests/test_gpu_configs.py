@@ -6,7 +6,6 @@ samples: forward rows (always including batch row 0's fully masked rows and
 the first rows that see keys again), whole heads for the backward (the oracle
 recomputes every statistic of that head itself), and every (batch, head) row
 of the decode."""
-import math
 
 import numpy as np
 import pytest
