@@ -111,3 +111,49 @@ def test_fp8_forward_persistent_many_units():
     # units in the second and third walk; all rows of four of them are held
     # to the bound, and every head's LSE is checked.
     _case(1, 64, 64, 1280, 1280, True, seed=86, qmul=8.0, heads=[0, 31, 47, 63])
+
+
+def test_fp8_forward_bench_workload_sampled_rows():
+    # The causal 8k workload the bench times (B=2 H=16 S=8192, Q x 8, batch
+    # row 0 keys 0..63 padded, so its first 64 query rows see no key),
+    # quantised per tensor: sampled rows, including the empty ones, are held
+    # to the element-wise bound and the LSE tolerance.
+    w = workloads.make("prefill_8k_masked")
+    t = w.tensors
+    q8, qd = _quant(t["q"])
+    k8, kd = _quant(t["k"])
+    v8, vd = _quant(t["v"])
+    vt8 = v8.transpose(-1, -2).contiguous()
+    kst, ken = t["k_start"], t["k_end"]
+    o, lse = fa.fa_fwd_fp8(q8.to(DEV), k8.to(DEV), vt8.to(DEV), True, w.scale, qd, kd, vd,
+                           k_start=kst.to(DEV), k_end=ken.to(DEV))
+    torch.cuda.synchronize()
+    st, word = fa.fa_device_status()
+    assert st == 0, hex(word)
+    B, Hq, S, d = t["q"].shape
+    Hkv = t["k"].shape[1]
+    must = [0, 63, 64, 65, 127, 128, 4095, S - 1, S + 5, 15 * S + 8000, (Hq + 3) * S + 64]
+    rows = np.array(sorted(set(must) | set(
+        int(x) for x in np.random.default_rng(87).integers(0, B * Hq * S, size=40))), np.int64)
+    qx = orc.decode_e4m3(q8) * qd
+    kx = orc.decode_e4m3(k8) * kd
+    vx = np.swapaxes(orc.decode_e4m3(vt8), -1, -2) * vd
+    ro, rl = orc.fwd(qx, kx, vx, True, w.scale, k_start=kst, k_end=ken, rows=rows)
+    got_o = to_np(o).reshape(-1, d)[rows]
+    check_lse(to_np(lse).reshape(-1)[rows], rl)
+    assert np.all(np.isfinite(got_o))
+    rep = Hq // Hkv
+    for n, r in enumerate(rows):
+        b, h, i = int(r) // (Hq * S), (int(r) // S) % Hq, int(r) % S
+        klo, khi = int(kst[b]), min(int(ken[b]), i + 1)  # causal, Sq == Sk
+        bound = 2.0 ** -8 * np.abs(ro[n]) + 1e-4
+        if khi > klo:
+            kk = kx[b, h // rep, klo:khi]
+            vv = vx[b, h // rep, klo:khi]
+            s = kk @ qx[b, h, i] * w.scale
+            pr = np.exp(s - s.max())
+            pr /= pr.sum()
+            dv_ = np.abs(vv - ro[n][None, :])
+            bound = bound + (2.0 ** -4 * (pr @ dv_) + 2.0 ** -10 * dv_.sum(axis=0)) / (1 - 2.0 ** -4)
+        worst = float((np.abs(got_o[n] - ro[n]) / bound).max())
+        assert worst <= 1.0, f"row {int(r)}: O error exceeds the e4m3 bound by {worst:.3f}x"
