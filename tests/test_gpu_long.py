@@ -1,5 +1,6 @@
-"""Long sequences (the largest sizes of this suite): the forward and backward at
-S = 65536 and 131072 against the FP64 oracle on sampled rows, and dK/dV
+"""Long sequences and full sizes: the forward and backward at S = 65536 and
+131072 against the FP64 oracle on sampled rows, the bench's key-mask and
+dropout rows on its full workload (sampled rows), and dK/dV
 through identities that hold at any size:
   sum over keys of dV_j = sum over query rows (that see a key) of dO_i,
     because each row of P sums to 1;
@@ -63,3 +64,35 @@ def test_backward_65536_sampled_rows_and_identities():
     dk_sum = to_np(dk)[0, 0].sum(axis=0)
     dk_abs = np.abs(to_np(dk)[0, 0]).sum(axis=0)
     assert np.all(np.abs(dk_sum) <= 2e-2 * dk_abs), float((np.abs(dk_sum) / dk_abs).max())
+
+
+@pytest.mark.parametrize("row_kind", ["key_mask", "dropout"])
+def test_bench_widened_rows_full_size_sampled(row_kind):
+    # The bench's widened rows on its own workload (B=2 H=16 S=8192, Q x 8,
+    # batch row 0 keys 0..63 padded): a seeded mask hiding 10% of the keys, or
+    # dropout p = 0.1; sampled rows (including rows that see no key) against
+    # the oracle.
+    w = workloads.make("prefill_8k_masked")
+    t = w.tensors
+    B, Hq, S, d = t["q"].shape
+    q, k, v = (t[n].to(DEV) for n in ("q", "k", "v"))
+    kst, ken = t["k_start"], t["k_end"]
+    kw = {}
+    okw = {}
+    if row_kind == "key_mask":
+        km = torch.rand(B, S, generator=torch.Generator().manual_seed(1)) >= 0.1
+        kw = dict(key_mask=km.to(DEV))
+        okw = dict(key_mask=km.numpy())
+    else:
+        kw = dict(dropout_p=0.1, seed=1, offset=0)
+        okw = dict(dropout_p=0.1, seed=1, offset=0)
+    o, lse = fa.fa_fwd(q, k, v, True, w.scale, k_start=kst.to(DEV), k_end=ken.to(DEV), **kw)
+    torch.cuda.synchronize()
+    st, word = fa.fa_device_status()
+    assert st == 0, hex(word)
+    rows = sample_rows(B, Hq, S, 48, seed=115,
+                       must=[0, 63, 64, 65, 128, S - 1, 5 * S + 4000, (Hq + 7) * S + 8191])
+    ro, rl = orc.fwd(t["q"], t["k"], t["v"], True, w.scale, k_start=kst, k_end=ken, rows=rows,
+                     **okw)
+    check_o(to_np(o).reshape(-1, d)[rows], ro)
+    check_lse(to_np(lse).reshape(-1)[rows], rl)
