@@ -96,3 +96,39 @@ def test_bench_widened_rows_full_size_sampled(row_kind):
                      **okw)
     check_o(to_np(o).reshape(-1, d)[rows], ro)
     check_lse(to_np(lse).reshape(-1)[rows], rl)
+
+
+def test_bench_varlen_full_size_sampled():
+    # The bench's packed lengths (the same seeded draw): 16 causal sequences of
+    # 1024..8192 tokens, H = 16, d = 128, seeded values; sampled packed rows
+    # against the oracle run on the row's own sequence.
+    g = torch.Generator().manual_seed(1)
+    torch.rand(2, 8192, generator=g)  # the bench draws its key mask first
+    lens = torch.randint(1024, 8193, (16,), generator=g)
+    cu = torch.zeros(17, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0)
+    total, H, d = int(cu[-1]), 16, 128
+    scale = 1.0 / math.sqrt(d)
+    gq = torch.Generator().manual_seed(2)
+    vq, vk, vv = (torch.randn(H, total, d, generator=gq).bfloat16() for _ in range(3))
+    cud = cu.to(DEV)
+    L = int(lens.max())
+    o, lse = fa.fa_fwd_varlen(vq.to(DEV), vk.to(DEV), vv.to(DEV), cud, cud, L, L, True, scale)
+    torch.cuda.synchronize()
+    st, word = fa.fa_device_status()
+    assert st == 0, hex(word)
+    rng = np.random.default_rng(116)
+    picks = [(0, 0), (H - 1, total - 1), (3, int(cu[5])), (7, int(cu[9]) - 1)]
+    picks += [(int(h), int(r)) for h, r in zip(rng.integers(0, H, 40), rng.integers(0, total, 40))]
+    got_o, ref_o, got_l, ref_l = [], [], [], []
+    for h, r in picks:
+        s = int(np.searchsorted(cu.numpy(), r, side="right")) - 1
+        a, b = int(cu[s]), int(cu[s + 1])
+        sl = lambda x: x[h:h + 1, a:b][None]  # noqa: E731  [1, 1, len, d]
+        ro, rl = orc.fwd(sl(vq), sl(vk), sl(vv), True, scale, rows=np.array([r - a]))
+        got_o.append(to_np(o[h, r])[None])
+        ref_o.append(ro)
+        got_l.append(np.array([float(lse[h, r])]))
+        ref_l.append(rl)
+    check_o(np.concatenate(got_o), np.concatenate(ref_o))
+    check_lse(np.concatenate(got_l), np.concatenate(ref_l))
